@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch: reshape_and_cache of
+the batch's new tokens, then paged attention over every sequence's cache
+(split-KV partitions + merge, and the read-once shared-prefix kernel for the
+shared-prefix workload).  Default workload: the 8B-shape decode batch (64
+sequences, 32 query / 8 kv heads, head_dim 128, block_size 16, contexts
+uniform in [512, 4096], blocks shuffled through a pool 1.25x the need).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the fp64 CPU oracle, same metric
+
+Prints one JSON line (rank 0).  ``value`` is KV-read GB/s of the whole step
+(algorithmic bytes: every (block, kv head) page a step must read, once, x the
+K and V page bytes) over the device time of K steps, summed over ranks; each
+rank runs its own replica (the path shards by sequence with no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "paged decode-attention KV-read GB/s vs GB300 HBM peak; seq-steps/sec"
+KERNEL_SOURCES = ["pa_attn.cuh", "pa_ptx.cuh", "pa_internal.h", "attn_d128.cu", "pa_misc.cu",
+                  "group_d128.cu"]
+WORKLOAD_DESC = {
+    "tiny": "2 seqs (ctx 37, 100), 4 q = 4 kv heads, head_dim 64, 16-block pool",
+    "decode_8b": "64 seqs, ctx uniform [512, 4096], 32 q / 8 kv heads, head_dim 128",
+    "decode_70b": "256 seqs, ctx log-uniform [128, 8192], 64 q / 8 kv heads, head_dim 128",
+    "spec_verify": "32 seqs x 5 drafts, ctx uniform [2048, 16384], 32 q / 8 kv heads",
+    "shared_prefix": "2 groups x 8 seqs sharing a 2048-token prefix, ctx 32768, 32 q / 8 kv "
+                     "heads, 512-token partitions",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0 = about 1.5 s worth)")
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="decode_8b")
+    ap.add_argument("--partition-size", type=int, default=-1,
+                    help="split-KV partition tokens (-1 = the workload's, 0 = library default)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_221_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from a committed ncu summary, if the
+    kernel sources have not changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_src_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(workload, seconds):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-m", "oracle.cpu_baseline", workload, str(seconds)],
+                       cwd=ROOT, env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"failed: {r.stderr.strip().splitlines()[-1:]}"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(d["gbps"], 4), "unit": "GB/s", "cores": d["cores"], "kind": "oracle",
+            "sample": d["sample"], "seconds": round(d["seconds"], 2),
+            "seq_steps_per_s": round(d["seq_steps_per_s"], 3)}
+
+
+def workload_config(w, ps, world):
+    return {"workload": w.name, "desc": WORKLOAD_DESC.get(w.name, w.name),
+            "num_seqs": w.num_seqs, "query_tokens": w.num_query_tokens,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "pool_blocks": w.num_blocks,
+            "partition_size": ps, "global_batch": w.num_seqs * world,
+            "l2": "inputs larger than L2: each step reads %.2f GB of a %.2f GB pool (L2 129 MB)"
+                  % (w.kv_bytes() / 1e9, 2 * w.k_cache.nbytes / 1e9),
+            "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    # Pin BLAS to one thread before NumPy loads.
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    sys.path.insert(0, ROOT)
+    from oracle import cpu_baseline as C
+
+    w, k, v = C.prepare(args.workload)
+    # per-step sample: enough whole sequences for ~0.5 s, fewer when many steps are asked
+    steps = args.steps if args.steps > 0 else 10
+    per_seq = max(C.run_seqs(w, k, v, [0]), 1e-4)
+    budget = 150.0 / max(1, steps + args.warmup)
+    n = max(1, min(w.num_seqs, int(min(0.5, budget) / per_seq)))
+    ring = list(range(w.num_seqs)) * 2
+
+    def sample(i):
+        s0 = (i * n) % w.num_seqs
+        return ring[s0:s0 + n]
+
+    for i in range(args.warmup):
+        C.run_seqs(w, k, v, sample(i))
+    nbytes = 0
+    nseq = 0
+    dt = 0.0
+    for i in range(steps):
+        sm = sample(i)
+        dt += C.run_seqs(w, k, v, sm)
+        nbytes += sum(C.seq_bytes(w, [b]) for b in sm)
+        nseq += len(sm)
+    gbps = nbytes / dt / 1e9
+    ps = w.partition_size
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbps, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)",
+            "config": workload_config(w, ps, 1),
+            "seq_steps_per_s": round(nseq / dt, 3),
+            "cpu_baseline": {"value": round(gbps, 4), "unit": "GB/s", "cores": C.threads_used(),
+                             "kind": "oracle",
+                             "sample": f"{n} whole sequence(s) of the {w.name} batch per step "
+                                       f"(fp64 paged attention, reshape untimed)"},
+            "e2e": {"value": round(gbps, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GB300 arm
+
+def run_gb300(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    sys.path.insert(0, ROOT)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import paged_kv_cache_221_gb300 as pa
+    import workloads as W
+
+    make = W.FULL[args.workload]
+    default_seed = make.__defaults__[0] if make.__defaults__ else 0
+    w = make(default_seed + 1000 * rank)
+    ps = w.partition_size if args.partition_size < 0 else args.partition_size
+
+    def td(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.to(dev)
+
+    q, k, v = td(w.q), td(w.k_cache), td(w.v_cache)
+    tables, lens = td(w.block_tables), td(w.context_lens)
+    nk, nv, slots = td(w.new_key), td(w.new_value), td(w.slot_mapping)
+    grouped = w.seq_group is not None
+    sg = td(w.seq_group) if grouped else None
+    gp = td(w.group_prefix_blocks) if grouped else None
+    T = w.num_query_tokens
+    need = pa.workspace_size(w.num_seqs, w.num_q_heads, T, w.max_context_len, w.head_dim, 16,
+                             ps, w.max_prefix_blocks if grouped else 0)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    kv_bytes = w.kv_bytes()
+
+    def reshape():
+        pa.reshape_and_cache(nk, nv, k, v, slots)
+
+    def attend():
+        if grouped:
+            pa.decode_shared_prefix(q, k, v, tables, lens, sg, gp, w.max_group_size,
+                                    w.max_prefix_blocks, w.max_context_len, w.scale, ps, ws, out)
+        else:
+            pa.verify(q, k, v, tables, lens, w.max_context_len, w.scale, ps, ws, out)
+
+    launches_per_step = 1 + 1 + (1 if need > 0 else 0) + (1 if grouped else 0)
+
+    stream = torch.cuda.current_stream(dev)
+    # warm-up outside capture (sets kernel attributes), then capture one graph per phase
+    for _ in range(max(3, args.warmup)):
+        reshape()
+        attend()
+    torch.cuda.synchronize(dev)
+    assert pa.get_device_error(dev) == 0
+    g_reshape, g_attend = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_reshape, stream=side):
+            reshape()
+        with torch.cuda.graph(g_attend, stream=side):
+            attend()
+    stream.wait_stream(side)
+    for _ in range(max(3, args.warmup)):
+        g_reshape.replay()
+        g_attend.replay()
+    torch.cuda.synchronize(dev)
+
+    # step count: about 1.5 s of timed work unless given
+    steps = args.steps
+    if steps <= 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            g_reshape.replay()
+            g_attend.replay()
+        e1.record(stream)
+        e1.synchronize()
+        per = e0.elapsed_time(e1) / 20
+        steps = int(max(50, min(20000, 1500.0 / max(per, 1e-3))))
+
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(steps):
+        g_reshape.replay()
+        ev_a[i].record(stream)
+        g_attend.replay()
+        ev_b[i].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    # keep sampling under the same load until there are enough samples
+    t_end = time.time() + 0.6
+    while time.time() < t_end:
+        for _ in range(50):
+            g_reshape.replay()
+            g_attend.replay()
+        torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    assert pa.get_device_error(dev) == 0, "device error during the timed region"
+
+    ms_total = start.elapsed_time(stop)
+    attn_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(steps)]
+    attn_avg = sum(attn_ms) / steps
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / steps
+    total_bytes = kv_bytes * world
+    value = total_bytes * steps / (ms_total * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host inputs in, output back, every step
+    e2e = None
+    if not args.no_e2e:
+        h = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for n, a in
+             (("q", w.q.view(np.int16)), ("nk", w.new_key.view(np.int16)),
+              ("nv", w.new_value.view(np.int16)), ("slots", w.slot_mapping),
+              ("tables", w.block_tables), ("lens", w.context_lens))}
+        d_in = {"q": q.view(torch.int16), "nk": nk.view(torch.int16), "nv": nv.view(torch.int16),
+                "slots": slots, "tables": tables, "lens": lens}
+        h_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+        bi = sum(t.numel() * t.element_size() for t in h.values())
+        bo = h_out.numel() * h_out.element_size()
+        e2e_steps = max(10, min(steps, 1000))
+        for _ in range(3):
+            for n_ in h:
+                d_in[n_].copy_(h[n_], non_blocking=True)
+            reshape()
+            attend()
+            h_out.copy_(out.view(torch.int16), non_blocking=True)
+        torch.cuda.synchronize(dev)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            for n_ in h:
+                d_in[n_].copy_(h[n_], non_blocking=True)
+            reshape()
+            attend()
+            h_out.copy_(out.view(torch.int16), non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = s0.elapsed_time(s1) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+               "path": "pinned host inputs -> H2D -> pa_reshape_and_cache + attention call "
+                       "(Python binding, no graph) -> D2H of the bf16 output"}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (attn_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)",
+        "config": workload_config(w, ps, world),
+        "seq_steps_per_s": round(w.num_seqs * world * steps / (ms_total * 1e-3), 1),
+        "kv_bytes_per_step": kv_bytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(w.name),
+                     "kernel": "attention call (paged_attn_kernel + splitkv_reduce_kernel)",
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "launch_ms_avg": round(attn_avg, 5),
+                     "launch_ms_median": round(statistics.median(attn_ms), 5)},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * steps,
+        "timing": "CUDA graphs of the two phases replayed per step; events on the launching "
+                  "stream",
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w.name, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gb300(args)
+
+
+if __name__ == "__main__":
+    main()

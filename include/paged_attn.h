@@ -1,0 +1,205 @@
+/*
+ * paged_attn.h — C ABI of the GB300 (sm_103a) paged decode-attention library.
+ *
+ * The KV cache of every sequence is cut into fixed-size physical blocks of
+ * `block_size` tokens (16) placed anywhere in one shared pool; a per-sequence
+ * block table maps logical token blocks to physical ones and is resolved on the
+ * fly inside the attention kernel ("PagedAttention, décodage spéculatif, MoE et
+ * Blackwell", §1, pagination de type système d'exploitation; "LLM inference
+ * optimization: KV cache", §4.1).
+ *
+ * Data layouts (all device pointers, row-major, contiguous, bf16 = IEEE
+ * bfloat16 stored as 2 bytes):
+ *   q, out        [num_seqs, num_query_tokens, num_q_heads, head_dim]   bf16
+ *   k_cache,
+ *   v_cache       [num_blocks, num_kv_heads, block_size, head_dim]      bf16
+ *                 (one (block, kv head) "page" of block_size*head_dim values
+ *                  is contiguous: 4 KB at head_dim 128)
+ *   block_tables  [num_seqs, max_blocks_per_seq]                        int32
+ *   context_lens  [num_seqs]                                            int32
+ *   key, value    [num_tokens, num_kv_heads, head_dim]                  bf16
+ *   slot_mapping  [num_tokens]   slot = physical_block*block_size+offset int64
+ *
+ * Conventions:
+ *   - context_lens[b] counts every cached token of sequence b INCLUDING its
+ *     num_query_tokens newest ones (the new decode token, or the drafts), whose
+ *     K/V must already have been written with pa_reshape_and_cache.
+ *   - Query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *   - Query token t of sequence b sees positions j <= context_lens[b] - T + t
+ *     (T = num_query_tokens; a causal mask among the drafts).
+ *   - Softmax statistics and accumulation are fp32; the output is rounded to
+ *     bf16 (round to nearest even) once.
+ *
+ * Ownership: the caller owns every buffer.  The library never allocates or
+ * frees device memory and keeps no per-call state; `workspace` is scratch the
+ * caller provides (its size comes from pa_workspace_size).
+ *
+ * Execution: every call only validates its arguments on the host, then
+ * enqueues kernels on `stream` and returns; it never synchronises (except
+ * pa_get_device_error, which says so).
+ *
+ * Errors: argument errors are returned synchronously and nothing is launched.
+ * A launch failure returns PA_ERR_CUDA.  Conditions only the device can see
+ * (a block id outside the pool, a slot outside the pool, a context length
+ * above max_context_len or below num_query_tokens, a pipeline wait that
+ * exceeded its time limit) set a sticky device error word; the affected work
+ * is skipped, never read or written out of bounds, and pa_get_device_error
+ * reports the condition.  Nothing throws across this ABI.
+ */
+#ifndef PAGED_ATTN_H
+#define PAGED_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t / CUstream; NULL = legacy default stream. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, misaligned pointer, ...      */
+  PA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim not 64/128, ...       */
+  PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pa_workspace_size */
+  PA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed                */
+  PA_ERR_BOUNDS = 5,        /* device saw a block id / slot / length out of range  */
+  PA_ERR_TIMEOUT = 6        /* device pipeline wait exceeded its limit             */
+} pa_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* pa_status_string(int status);
+
+/* ABI version of this library (major*100 + minor). */
+int pa_version(void);
+
+/*
+ * pa_reshape_and_cache — store the K and V vectors of `num_tokens` new tokens
+ * into their cache slots: for token i with s = slot_mapping[i] >= 0,
+ *   k_cache[s / block_size, h, s % block_size, :] = key[i, h, :]   for all h
+ * and the same for V.  A negative slot marks a padding token and is skipped.
+ * Bits are copied unchanged (bit-exact).  Two tokens naming the same slot leave
+ * that slot holding one of them (which one is unspecified).
+ * Cited: "LLM inference optimization: KV cache", §3.1 (the new token's K and V
+ * are saved into the KV cache); the slot arithmetic follows from the block
+ * layout above.
+ * Requirements: all pointers non-NULL and 16-byte aligned, head_dim a multiple
+ * of 8, block_size 16.  A slot >= num_blocks*block_size sets PA_ERR_BOUNDS on
+ * the device and that token is skipped.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                               void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                               int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                               pa_stream_t stream);
+
+/*
+ * pa_workspace_size — bytes of scratch the attention calls need for split-KV
+ * partials with these sizes (0 if no sequence can need more than one
+ * partition).  partition_size = 0 selects the library default, exactly as the
+ * attention calls do.  max_prefix_blocks is 0 for pa_decode / pa_verify.
+ */
+size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_query_tokens,
+                         int max_context_len, int head_dim, int block_size, int partition_size,
+                         int max_prefix_blocks);
+
+/* Partition size (tokens) that partition_size = 0 selects for this shape. */
+int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_len,
+                              int block_size);
+
+/*
+ * pa_decode — single-token paged decode attention (num_query_tokens = 1):
+ *   out[b, 0, h, :] = sum_j softmax_j(scale * q[b,0,h,:] . K_j) V_j
+ * over the context_lens[b] cached positions j of sequence b, K_j / V_j read
+ * from page block_tables[b, j / block_size], slot j % block_size, kv head
+ * h / (Hq/Hkv).  Cited: "LLM inference optimization: KV cache", §3.1 (attention
+ * from the new token's Q over the cached K, V) and §4.1 (block table);
+ * "PagedAttention, ..." §1.
+ *
+ * Long contexts are split into partitions of partition_size tokens (0 = the
+ * library default) that are processed in parallel and merged with the
+ * log-sum-exp rule; this needs `workspace` of at least pa_workspace_size(...)
+ * bytes.  With partition_size = 0 and workspace == NULL every sequence is
+ * processed whole (no scratch, fewer parallel units).  With an explicit
+ * partition_size that needs scratch, a missing or short workspace returns
+ * PA_ERR_WORKSPACE.
+ *
+ * max_context_len must bound every context_lens[b] and be at most
+ * max_blocks_per_seq*block_size; it sizes the launch without a device read.
+ * Requirements: head_dim 64 or 128, block_size 16, num_q_heads a multiple of
+ * num_kv_heads with at most 64 query heads per kv head, q/out/k_cache/v_cache
+ * 16-byte aligned, num_blocks*num_kv_heads*block_size < 2^31.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int max_context_len, int num_seqs,
+                    int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                    int block_size, float scale, int partition_size, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_verify — speculative-decoding verification: the num_query_tokens (T)
+ * draft tokens of every sequence attend over the paged cache in one pass,
+ * draft t seeing positions j <= context_lens[b] - T + t (causal mask among the
+ * drafts, whose K/V occupy the last T positions).  Cited: "PagedAttention, ..."
+ * §1 (vérification parallèle of K drafts in one forward pass); "LLM inference
+ * optimization: KV cache", §5.2.  Other arguments as pa_decode; requires
+ * 1 <= T and (num_q_heads/num_kv_heads) * T <= 64.
+ */
+pa_status pa_verify(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int max_context_len, int num_seqs,
+                    int num_query_tokens, int num_blocks, int num_q_heads, int num_kv_heads,
+                    int head_dim, int block_size, float scale, int partition_size,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode_shared_prefix — pa_decode for batches where groups of sequences
+ * share their first blocks copy-on-write (one prompt, several beams or
+ * parallel completions point at the same physical blocks: "PagedAttention,
+ * ..." §1, partage de mémoire; "LLM inference optimization: KV cache", §4.2).
+ * The shared pages of a group are read from memory once per kv head for all
+ * members of the group together; the members' private pages are read per
+ * sequence; all partial results are merged per sequence.  The result equals
+ * pa_decode on the same tables.
+ *
+ *   seq_group[b]            group of sequence b, or -1 if it shares nothing
+ *   group_prefix_blocks[g]  number of leading block-table entries that are
+ *                           identical in the tables of every member of g
+ *   max_group_size          upper bound on members per group (host-side sizing)
+ *   max_prefix_blocks       upper bound on group_prefix_blocks[g]
+ * Every member must have context_lens[b] >= group_prefix_blocks[g]*block_size.
+ * Requires a workspace of pa_workspace_size(..., max_prefix_blocks) bytes.
+ */
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_tables,
+                                  int max_blocks_per_seq, const int32_t* context_lens,
+                                  int max_context_len, int num_seqs, int num_blocks,
+                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, float scale, int partition_size,
+                                  const int32_t* seq_group, const int32_t* group_prefix_blocks,
+                                  int num_groups, int max_group_size, int max_prefix_blocks,
+                                  void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_get_device_error — synchronise `stream`, then return and clear the sticky
+ * device error word: PA_ERR_TIMEOUT if any pipeline wait gave up, else
+ * PA_ERR_BOUNDS if any out-of-range id, slot or length was seen, else PA_OK
+ * (PA_ERR_CUDA if the synchronisation itself failed).
+ */
+pa_status pa_get_device_error(pa_stream_t stream);
+
+/*
+ * pa_selftest_wait_timeout — failure-detection self test.  Launches one CTA
+ * that waits on a shared-memory barrier nothing ever signals, with a limit of
+ * timeout_ns nanoseconds (1000 .. 10^9); the wait gives up, records
+ * PA_ERR_TIMEOUT in the device error word and the kernel returns normally.
+ * Read the result with pa_get_device_error.  Nothing faults or hangs.
+ */
+pa_status pa_selftest_wait_timeout(unsigned long long timeout_ns, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGED_ATTN_H */

@@ -1,0 +1,90 @@
+"""Time the fp64 oracle, as it stands, on a bounded sample of a named workload.
+
+TEST INFRASTRUCTURE ONLY: used by the benchmark's CPU-baseline leg and its
+``--impl reference`` arm.  Run as a module in a child process so that the
+BLAS thread count can be pinned before NumPy loads:
+
+    OPENBLAS_NUM_THREADS=1 OMP_NUM_THREADS=1 python -m oracle.cpu_baseline decode_8b 10
+
+prints one JSON object: KV bytes read by the oracle (unique pages of the
+sequences it processed), seconds, GB/s and the sample description.  The
+workload's new tokens are scattered into the caches before timing; the timed
+work is the oracle's paged attention over whole sequences, in batch order,
+repeated over the batch until ``seconds`` have elapsed.
+"""
+from __future__ import annotations
+
+import json
+import os
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+from oracle import oracle as O  # noqa: E402
+
+
+def threads_used() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "") != "1":
+            return len(os.sched_getaffinity(0))
+    return 1
+
+
+def prepare(name: str):
+    w = W.FULL[name]()
+    k, v = O.reshape_and_cache(w.new_key, w.new_value, w.k_cache, w.v_cache, w.slot_mapping,
+                               w.block_size)
+    return w, k, v
+
+
+def seq_bytes(w, seqs) -> int:
+    used = set()
+    for b in seqs:
+        nblk = -(-int(w.context_lens[b]) // w.block_size)
+        used.update(int(x) for x in w.block_tables[b, :nblk])
+    return len(used) * w.num_kv_heads * w.page_bytes()
+
+
+def run_seqs(w, k, v, seqs):
+    """Oracle attention over exactly ``seqs``, one sequence at a time; returns seconds."""
+    t0 = time.perf_counter()
+    for b in seqs:
+        O.paged_attention(w.q, k, v, w.block_tables, w.context_lens, w.scale, w.num_kv_heads,
+                          w.block_size, seqs=[b])
+    return time.perf_counter() - t0
+
+
+def time_passes(w, k, v, seconds: float):
+    """Oracle passes over the batch, one sequence at a time, until ``seconds`` elapsed."""
+    done = []
+    t0 = time.perf_counter()
+    b = 0
+    while not done or time.perf_counter() - t0 < seconds:
+        run_seqs(w, k, v, [b])
+        done.append(b)
+        b = (b + 1) % w.num_seqs
+    dt = time.perf_counter() - t0
+    nbytes = sum(seq_bytes(w, [x]) for x in done)
+    return {"bytes": nbytes, "seconds": dt, "gbps": nbytes / dt / 1e9, "seqs": len(done),
+            "seq_steps_per_s": len(done) / dt}
+
+
+def main(argv):
+    name = argv[1] if len(argv) > 1 else "decode_8b"
+    seconds = float(argv[2]) if len(argv) > 2 else 10.0
+    w, k, v = prepare(name)
+    r = time_passes(w, k, v, seconds)
+    r.update({"workload": name, "cores": threads_used(),
+              "sample": f"{r['seqs']} whole sequences of the {name} batch (batch order, "
+                        f"wrapping), fp64 paged attention; reshape_and_cache untimed"})
+    print(json.dumps(r))
+
+
+if __name__ == "__main__":
+    main(sys.argv)

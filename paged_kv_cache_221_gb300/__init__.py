@@ -1,0 +1,211 @@
+"""GB300-native paged decode attention.
+
+A thin PyTorch binding over the C ABI of ``libpaged_attn.so`` (declared in
+``include/paged_attn.h``).  This module only checks tensor shapes, dtypes and
+devices and marshals pointers and the current CUDA stream; every step of the
+computation runs in the library's sm_103a kernels.  PyTorch is used for device
+memory and streams only.
+
+Layouts (bf16 unless stated):
+    q, out        [num_seqs, num_query_tokens, num_q_heads, head_dim]
+    k_cache,
+    v_cache       [num_blocks, num_kv_heads, block_size, head_dim]
+    block_tables  [num_seqs, max_blocks_per_seq] int32
+    context_lens  [num_seqs] int32 (counts the newest token / the drafts)
+    key, value    [num_tokens, num_kv_heads, head_dim]
+    slot_mapping  [num_tokens] int64
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import PagedAttnError, STATUS_NAMES
+
+__all__ = ["reshape_and_cache", "decode", "verify", "decode_shared_prefix", "workspace_size",
+           "default_partition_size", "get_device_error", "selftest_wait_timeout", "library",
+           "PagedAttnError", "STATUS_NAMES"]
+
+
+def library() -> ctypes.CDLL:
+    """The loaded ``libpaged_attn.so`` (raises ImportError if it was not built)."""
+    return _lib.load()
+
+
+def _vp(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(dev: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _need(name, t, dtype, ndim, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, slot_mapping: torch.Tensor) -> None:
+    """Scatter new K/V rows into their cache slots (in place, bit-exact)."""
+    _need("k_cache", k_cache, torch.bfloat16, 4)
+    dev = k_cache.device
+    _need("v_cache", v_cache, torch.bfloat16, 4, dev)
+    _need("key", key, torch.bfloat16, 3, dev)
+    _need("value", value, torch.bfloat16, 3, dev)
+    _need("slot_mapping", slot_mapping, torch.int64, 1, dev)
+    NB, Hkv, BS, D = k_cache.shape
+    N = key.shape[0]
+    if v_cache.shape != k_cache.shape or key.shape != (N, Hkv, D) or value.shape != key.shape \
+            or slot_mapping.shape[0] != N:
+        raise ValueError("inconsistent shapes")
+    st = library().pa_reshape_and_cache(_vp(key), _vp(value), _vp(k_cache), _vp(v_cache),
+                                        _vp(slot_mapping), N, NB, Hkv, D, BS, _stream(dev))
+    _lib.check("pa_reshape_and_cache", st)
+
+
+def workspace_size(num_seqs: int, num_q_heads: int, num_query_tokens: int, max_context_len: int,
+                   head_dim: int, block_size: int = 16, partition_size: int = 0,
+                   max_prefix_blocks: int = 0) -> int:
+    """Scratch bytes an attention call with these sizes needs (0 if none)."""
+    return int(library().pa_workspace_size(num_seqs, num_q_heads, num_query_tokens,
+                                           max_context_len, head_dim, block_size, partition_size,
+                                           max_prefix_blocks))
+
+
+def default_partition_size(num_seqs: int, num_kv_heads: int, max_context_len: int,
+                           block_size: int = 16) -> int:
+    return int(library().pa_default_partition_size(num_seqs, num_kv_heads, max_context_len,
+                                                   block_size))
+
+
+def _attn_common(q, k_cache, v_cache, block_tables, context_lens, max_context_len, out):
+    _need("k_cache", k_cache, torch.bfloat16, 4)
+    dev = k_cache.device
+    _need("v_cache", v_cache, torch.bfloat16, 4, dev)
+    _need("q", q, torch.bfloat16, 4, dev)
+    _need("block_tables", block_tables, torch.int32, 2, dev)
+    _need("context_lens", context_lens, torch.int32, 1, dev)
+    B, T, Hq, D = q.shape
+    NB, Hkv, BS, Dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or Dk != D or block_tables.shape[0] != B or \
+            context_lens.shape[0] != B:
+        raise ValueError("inconsistent shapes")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else T   # host sync
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need("out", out, torch.bfloat16, 4, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    return dev, B, T, Hq, D, NB, Hkv, BS, int(max_context_len), out
+
+
+def _workspace(dev, workspace, need):
+    if workspace is None:
+        if need == 0:
+            return None, 0
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    elif not (workspace.is_cuda and workspace.device == dev and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor on the cache's device")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+           block_tables: torch.Tensor, context_lens: torch.Tensor,
+           max_context_len: Optional[int] = None, scale: Optional[float] = None,
+           partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Attention of T draft tokens per sequence ([B, T, Hq, D]) with a causal mask among drafts."""
+    dev, B, T, Hq, D, NB, Hkv, BS, mcl, out = _attn_common(q, k_cache, v_cache, block_tables,
+                                                          context_lens, max_context_len, out)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    need = workspace_size(B, Hq, T, mcl, D, BS, partition_size, 0) if B else 0
+    ws, wsb = _workspace(dev, workspace, need)
+    lib = library()
+    if T == 1:
+        st = lib.pa_decode(_vp(out), _vp(q), _vp(k_cache), _vp(v_cache), _vp(block_tables),
+                           block_tables.shape[1], _vp(context_lens), mcl, B, NB, Hq, Hkv, D, BS,
+                           scale, partition_size, _vp(ws), wsb, _stream(dev))
+        _lib.check("pa_decode", st)
+    else:
+        st = lib.pa_verify(_vp(out), _vp(q), _vp(k_cache), _vp(v_cache), _vp(block_tables),
+                           block_tables.shape[1], _vp(context_lens), mcl, B, T, NB, Hq, Hkv, D,
+                           BS, scale, partition_size, _vp(ws), wsb, _stream(dev))
+        _lib.check("pa_verify", st)
+    return out
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+           block_tables: torch.Tensor, context_lens: torch.Tensor,
+           max_context_len: Optional[int] = None, scale: Optional[float] = None,
+           partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Single-token decode attention; q is [B, Hq, D] or [B, 1, Hq, D] (out has q's shape)."""
+    squeeze = q.dim() == 3
+    q4 = q.unsqueeze(1) if squeeze else q
+    if q4.shape[1] != 1:
+        raise ValueError("decode takes one query token per sequence (use verify for drafts)")
+    o4 = None if out is None else (out.unsqueeze(1) if squeeze else out)
+    r = verify(q4, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+               partition_size, workspace, o4)
+    return r.squeeze(1) if squeeze else r
+
+
+def decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         block_tables: torch.Tensor, context_lens: torch.Tensor,
+                         seq_group: torch.Tensor, group_prefix_blocks: torch.Tensor,
+                         max_group_size: int, max_prefix_blocks: int,
+                         max_context_len: Optional[int] = None, scale: Optional[float] = None,
+                         partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                         out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode where groups of sequences share copy-on-write prefix blocks, read once per group."""
+    squeeze = q.dim() == 3
+    q4 = q.unsqueeze(1) if squeeze else q
+    o4 = None if out is None else (out.unsqueeze(1) if squeeze else out)
+    dev, B, T, Hq, D, NB, Hkv, BS, mcl, o4 = _attn_common(q4, k_cache, v_cache, block_tables,
+                                                         context_lens, max_context_len, o4)
+    if T != 1:
+        raise ValueError("decode_shared_prefix takes one query token per sequence")
+    _need("seq_group", seq_group, torch.int32, 1, dev)
+    _need("group_prefix_blocks", group_prefix_blocks, torch.int32, 1, dev)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    need = workspace_size(B, Hq, 1, mcl, D, BS, partition_size, max_prefix_blocks) if B else 0
+    ws, wsb = _workspace(dev, workspace, need)
+    st = library().pa_decode_shared_prefix(
+        _vp(o4), _vp(q4), _vp(k_cache), _vp(v_cache), _vp(block_tables), block_tables.shape[1],
+        _vp(context_lens), mcl, B, NB, Hq, Hkv, D, BS, scale, partition_size, _vp(seq_group),
+        _vp(group_prefix_blocks), group_prefix_blocks.shape[0], max_group_size,
+        max_prefix_blocks, _vp(ws), wsb, _stream(dev))
+    _lib.check("pa_decode_shared_prefix", st)
+    return o4.squeeze(1) if squeeze else o4
+
+
+def get_device_error(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device error status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    return int(library().pa_get_device_error(_stream(dev)))
+
+
+def selftest_wait_timeout(timeout_ns: int, device=None) -> None:
+    """Launch the bounded-wait self test (read the outcome with get_device_error)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    _lib.check("pa_selftest_wait_timeout",
+               library().pa_selftest_wait_timeout(int(timeout_ns), _stream(dev)))

@@ -1,0 +1,67 @@
+"""ctypes declarations of the C ABI in ``include/paged_attn.h``.
+
+Loading fails loudly if ``libpaged_attn.so`` has not been built: there is no
+fallback implementation of any operation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpaged_attn.so")
+
+PA_OK = 0
+STATUS_NAMES = {
+    0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
+    4: "PA_ERR_CUDA", 5: "PA_ERR_BOUNDS", 6: "PA_ERR_TIMEOUT",
+}
+
+# Every symbol the header declares, with (restype, argtypes).
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "pa_status_string": (ctypes.c_char_p, [_i]),
+    "pa_version": (_i, []),
+    "pa_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "pa_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "pa_default_partition_size": (_i, [_i, _i, _i, _i]),
+    "pa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i,
+                       _vp, _sz, _vp]),
+    "pa_verify": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
+                       _i, _vp, _sz, _vp]),
+    "pa_decode_shared_prefix": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                                     _i, _f, _i, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+    "pa_get_device_error": (_i, [_vp]),
+    "pa_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
+}
+
+_lib = None
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library (once) and declare every entry point."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; "
+            f"g.build()' or python paged_kv_cache_221_gb300/build.py)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def check(fn: str, status: int) -> None:
+    if status != PA_OK:
+        raise PagedAttnError(fn, status)

@@ -1,0 +1,330 @@
+// C ABI of the paged decode-attention library: argument checks, split-KV
+// planning, TMA descriptor encoding and kernel launches on the caller's stream.
+// No call allocates device memory or synchronises (pa_get_device_error aside).
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/paged_attn.h"
+#include "pa_internal.h"
+
+using namespace pa;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// The pool [num_blocks, Hkv, 16, D] viewed as a 2-D tensor of rows of D bf16;
+// a 16 x 64 box lands in shared memory with the 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* base, long long rows, int head_dim) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Plan {
+  int ppb = 1;           // pages per partition
+  int max_parts = 1;     // partition slots per query row
+  size_t ws_bytes = 0;   // scratch needed
+  size_t off_m = 0, off_l = 0;
+};
+
+int default_partition_tokens(int max_context_len) {
+  return max_context_len > 512 ? 512 : ceil_div(max_context_len, kBlockSize) * kBlockSize;
+}
+
+Plan make_plan(int num_seqs, int hq, int T, int max_ctx, int head_dim, int partition_size,
+               int max_prefix_blocks) {
+  Plan pl;
+  const int max_blocks = ceil_div(max_ctx, kBlockSize);
+  pl.ppb = partition_size / kBlockSize;
+  if (pl.ppb < 1) pl.ppb = 1;
+  pl.max_parts = ceil_div(max_prefix_blocks, pl.ppb) + ceil_div(max_blocks, pl.ppb);
+  if (pl.max_parts < 1) pl.max_parts = 1;
+  if (pl.max_parts == 1 && max_prefix_blocks == 0) return pl;   // no scratch
+  const size_t rows = static_cast<size_t>(num_seqs) * T * hq;
+  const size_t po = round256(rows * pl.max_parts * head_dim * sizeof(float));
+  const size_t pm = round256(rows * pl.max_parts * sizeof(float));
+  pl.off_m = po;
+  pl.off_l = po + pm;
+  pl.ws_bytes = po + 2 * pm;
+  return pl;
+}
+
+struct AttnArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int max_context_len;
+  int num_seqs, T, num_blocks, hq, hkv, head_dim, block_size;
+  float scale;
+  int partition_size;
+  const int32_t* seq_group;
+  const int32_t* group_prefix_blocks;
+  int num_groups, max_group_size, max_prefix_blocks;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+pa_status run_attention(const AttnArgs& a) {
+  if (a.num_seqs < 0 || a.T < 1 || a.hq < 1 || a.hkv < 1 || a.num_blocks < 1 ||
+      a.max_blocks_per_seq < 1 || a.partition_size < 0)
+    return PA_ERR_INVALID_ARG;
+  if (a.num_seqs == 0) return PA_OK;
+  if (!a.out || !a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(a.out) || !aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache))
+    return PA_ERR_INVALID_ARG;
+  if (a.hq % a.hkv != 0) return PA_ERR_INVALID_ARG;
+  if (a.head_dim != 64 && a.head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (a.block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  const int G = a.hq / a.hkv;
+  if (static_cast<long long>(G) * a.T > kMaxRows) return PA_ERR_UNSUPPORTED;
+  if (a.max_context_len < a.T ||
+      static_cast<long long>(a.max_context_len) >
+          static_cast<long long>(a.max_blocks_per_seq) * kBlockSize)
+    return PA_ERR_INVALID_ARG;
+  if (a.partition_size % kBlockSize != 0) return PA_ERR_INVALID_ARG;
+  if (a.num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(a.num_blocks) * a.hkv * kBlockSize;
+  if (rows >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+  const bool grouped = a.num_groups > 0;
+  if (grouped) {
+    if (!a.seq_group || !a.group_prefix_blocks || a.max_group_size < 1 ||
+        a.max_prefix_blocks < 0 ||
+        static_cast<long long>(a.max_prefix_blocks) * kBlockSize > a.max_context_len)
+      return PA_ERR_INVALID_ARG;
+    if (static_cast<long long>(G) * a.T > kMaxRows) return PA_ERR_UNSUPPORTED;
+  }
+  const int max_prefix = grouped ? a.max_prefix_blocks : 0;
+
+  int psize = a.partition_size;
+  if (psize == 0) {
+    psize = default_partition_tokens(a.max_context_len);
+    Plan probe = make_plan(a.num_seqs, a.hq, a.T, a.max_context_len, a.head_dim, psize,
+                           max_prefix);
+    if (!grouped && probe.ws_bytes > 0 && a.workspace == nullptr)
+      psize = ceil_div(a.max_context_len, kBlockSize) * kBlockSize;   // whole sequences
+  }
+  const Plan plan = make_plan(a.num_seqs, a.hq, a.T, a.max_context_len, a.head_dim, psize,
+                              max_prefix);
+  if (plan.ws_bytes > 0) {
+    if (!a.workspace || a.workspace_bytes < plan.ws_bytes) return PA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(a.workspace) & 255u) return PA_ERR_INVALID_ARG;
+  }
+
+  CUtensorMap tk, tv;
+  if (!encode_pool_map(&tk, a.k_cache, rows, a.head_dim) ||
+      !encode_pool_map(&tv, a.v_cache, rows, a.head_dim))
+    return PA_ERR_CUDA;
+
+  AttnParams p{};
+  p.q = a.q;
+  p.out = a.out;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  if (plan.ws_bytes > 0) {
+    char* ws = static_cast<char*>(a.workspace);
+    p.part_o = reinterpret_cast<float*>(ws);
+    p.part_m = reinterpret_cast<float*>(ws + plan.off_m);
+    p.part_l = reinterpret_cast<float*>(ws + plan.off_l);
+  }
+  p.seq_group = grouped ? a.seq_group : nullptr;
+  p.group_prefix_blocks = grouped ? a.group_prefix_blocks : nullptr;
+  p.mbs = a.max_blocks_per_seq;
+  p.max_ctx = a.max_context_len;
+  p.num_seqs = a.num_seqs;
+  p.T = a.T;
+  p.Hq = a.hq;
+  p.Hkv = a.hkv;
+  p.G = G;
+  p.num_blocks = a.num_blocks;
+  p.ppb = plan.ppb;
+  p.max_parts = plan.max_parts;
+  p.max_prefix_blocks = max_prefix;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.timeout_ns = kDefaultTimeoutNs;
+
+  const int max_blocks = ceil_div(a.max_context_len, kBlockSize);
+  cudaError_t e = cudaSuccess;
+  if (grouped && a.max_prefix_blocks > 0) {
+    const int mc = std::min(a.max_group_size, kMaxRows / (G * a.T));
+    p.members_per_chunk = mc;
+    p.num_chunks = ceil_div(a.max_group_size, mc);
+    const long long gz = static_cast<long long>(a.num_groups) * p.num_chunks;
+    if (gz > 65535) return PA_ERR_UNSUPPORTED;
+    const int ntw = ceil_div(static_cast<long long>(mc) * G * a.T, 8);
+    dim3 grid(ceil_div(a.max_prefix_blocks, plan.ppb), a.hkv, static_cast<unsigned>(gz));
+    e = a.head_dim == 64 ? launch_attn_group_d64(tk, tv, p, ntw, grid, a.stream)
+                         : launch_attn_group_d128(tk, tv, p, ntw, grid, a.stream);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  {
+    const int ntw = ceil_div(static_cast<long long>(G) * a.T, 8);
+    dim3 grid(ceil_div(max_blocks, plan.ppb), a.hkv, a.num_seqs);
+    e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, ntw, false, grid, a.stream)
+                         : launch_attn_d128(tk, tv, p, ntw, false, grid, a.stream);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  if (plan.ws_bytes > 0) {
+    e = launch_reduce(p, a.head_dim, a.stream);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_BOUNDS: return "PA_ERR_BOUNDS";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+    default: return "PA_ERR_UNKNOWN";
+  }
+}
+
+int pa_version(void) { return 100; }
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                               void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                               int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                               pa_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 ||
+      head_dim % 8 != 0)
+    return PA_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const cudaError_t e =
+      launch_reshape(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
+                     num_kv_heads, head_dim, block_size, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_len,
+                              int block_size) {
+  (void)num_seqs;
+  (void)num_kv_heads;
+  (void)block_size;
+  if (max_context_len < 1) return kBlockSize;
+  return default_partition_tokens(max_context_len);
+}
+
+size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_query_tokens,
+                         int max_context_len, int head_dim, int block_size, int partition_size,
+                         int max_prefix_blocks) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_query_tokens <= 0 || max_context_len <= 0 ||
+      head_dim <= 0 || block_size != kBlockSize || partition_size < 0 || max_prefix_blocks < 0)
+    return 0;
+  const int psize = partition_size == 0 ? default_partition_tokens(max_context_len)
+                                        : partition_size;
+  return make_plan(num_seqs, num_q_heads, num_query_tokens, max_context_len, head_dim, psize,
+                   max_prefix_blocks)
+      .ws_bytes;
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int max_context_len, int num_seqs,
+                    int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                    int block_size, float scale, int partition_size, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream) {
+  AttnArgs a{out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+             max_context_len, num_seqs, 1, num_blocks, num_q_heads, num_kv_heads, head_dim,
+             block_size, scale, partition_size, nullptr, nullptr, 0, 0, 0, workspace,
+             workspace_bytes, reinterpret_cast<cudaStream_t>(stream)};
+  return run_attention(a);
+}
+
+pa_status pa_verify(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int max_context_len, int num_seqs,
+                    int num_query_tokens, int num_blocks, int num_q_heads, int num_kv_heads,
+                    int head_dim, int block_size, float scale, int partition_size,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  AttnArgs a{out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+             max_context_len, num_seqs, num_query_tokens, num_blocks, num_q_heads, num_kv_heads,
+             head_dim, block_size, scale, partition_size, nullptr, nullptr, 0, 0, 0, workspace,
+             workspace_bytes, reinterpret_cast<cudaStream_t>(stream)};
+  return run_attention(a);
+}
+
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_tables,
+                                  int max_blocks_per_seq, const int32_t* context_lens,
+                                  int max_context_len, int num_seqs, int num_blocks,
+                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, float scale, int partition_size,
+                                  const int32_t* seq_group, const int32_t* group_prefix_blocks,
+                                  int num_groups, int max_group_size, int max_prefix_blocks,
+                                  void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (num_groups < 0) return PA_ERR_INVALID_ARG;
+  AttnArgs a{out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+             max_context_len, num_seqs, 1, num_blocks, num_q_heads, num_kv_heads, head_dim,
+             block_size, scale, partition_size, seq_group, group_prefix_blocks, num_groups,
+             max_group_size, max_prefix_blocks, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream)};
+  return run_attention(a);
+}
+
+pa_status pa_get_device_error(pa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  unsigned bits = 0;
+  if (take_error_attn_d64(&bits) != cudaSuccess || take_error_attn_d128(&bits) != cudaSuccess ||
+      take_error_group_d64(&bits) != cudaSuccess ||
+      take_error_group_d128(&bits) != cudaSuccess || take_error_misc(&bits) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (bits & kErrTimeout) return PA_ERR_TIMEOUT;
+  if (bits & kErrBounds) return PA_ERR_BOUNDS;
+  return PA_OK;
+}
+
+pa_status pa_selftest_wait_timeout(unsigned long long timeout_ns, pa_stream_t stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return PA_ERR_INVALID_ARG;
+  return launch_selftest_wait(timeout_ns, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+}  // extern "C"

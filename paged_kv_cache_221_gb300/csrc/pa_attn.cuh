@@ -1,0 +1,476 @@
+// Paged decode / verify attention kernel template (sm_103a).
+//
+// One CTA owns one work unit: (partition of one sequence's pages, kv head) in
+// the per-sequence mode, or (partition of a group's shared prefix pages, kv
+// head, chunk of group members) in the shared-prefix mode.  The block table
+// is resolved on the fly: a producer warp reads the physical block id of each
+// logical page and issues two-dimensional TMA loads of the K page and the V
+// page (block_size x head_dim bf16 each, contiguous in the pool) into a ring
+// of kStages shared-memory stages with 128-byte swizzle.  Consumer warps then
+// compute, per page, the scores of all query rows that read this kv head (the
+// GQA group x the query tokens, and in shared-prefix mode x the members) on
+// the tensor cores, an online softmax in fp32, and the P.V accumulation on the
+// tensor cores with P split into two bf16 halves so that P keeps ~16
+// significant bits.  Each page is read from HBM once per CTA.
+//
+// Tile orientation: tokens are the M dimension of the score tile
+// (S^T[16 tokens x 8 rows] = K_page[16 x D] . Q^T[D x 8]) and head dims are the
+// M dimension of the output tile (O^T[D x 8] += V_page^T[D x 16] . P^T[16 x 8]),
+// so a 16-token page is exactly one m16n8k16 step and the query rows of the
+// CTA (1 .. 64) fill the N = 8 side, one n-tile per consumer-warp column.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+template <int D>
+struct Geo {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kHalves = D / 64;                // 128-byte swizzle rows per token
+  static constexpr int kHalfBytes = kBlockSize * 128;   // one 16 x 64 bf16 TMA box
+  static constexpr int kPageBytes = kHalves * kHalfBytes;
+  static constexpr int kStageBytes = 2 * kPageBytes;    // K page + V page
+  static constexpr int kQStride = D + 8;                // bf16 per Q row in smem (conflict-free)
+  static constexpr int kOStride = D + 4;                // floats per merge row (conflict-free)
+  static constexpr int kKSteps = D / 16;
+};
+
+template <int D, int NTW>
+struct Smem {
+  static constexpr int kRows = 8 * NTW;
+  static constexpr int kStagesOff = 0;
+  static constexpr int kQOff = kStages * Geo<D>::kStageBytes;
+  static constexpr int kLimOff = kQOff + kRows * Geo<D>::kQStride * 2;
+  static constexpr int kBarOff = (kLimOff + kRows * 4 + 7) / 8 * 8;
+  static constexpr int kOkOff = kBarOff + 2 * kStages * 8;
+  static constexpr int kMemOff = kOkOff + kStages * 4;
+  static constexpr int kBytes = kMemOff + kMaxRows * 4;
+  static constexpr int kAlloc = kBytes + 1024;          // room to align the base to 1 KB
+  // merge buffers (reuse the stage ring once every page is consumed)
+  static constexpr int kMergeFloats = 16 + 8 * Geo<D>::kOStride;
+};
+
+// Byte offset of 16-byte chunk `ch` (of D/8) of token row `tok` inside one
+// swizzled page: two-dimensional TMA boxes of 16 rows x 128 bytes, 16-byte
+// chunk c of row r stored at chunk c ^ (r % 8).
+__device__ __forceinline__ uint32_t page_off(int tok, int ch) {
+  return static_cast<uint32_t>((ch >> 3) * (kBlockSize * 128) + tok * 128 +
+                               (((ch & 7) ^ (tok & 7)) << 4));
+}
+
+template <int D, int NTW, bool GROUP>
+__global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
+    paged_attn_kernel(const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+  constexpr int PL = page_lanes_for(NTW);
+  constexpr int NCW = NTW * PL;              // consumer warps
+  constexpr int NCT = NCW * 32;              // consumer threads
+  using Gm = Geo<D>;
+  using Sm = Smem<D, NTW>;
+  static_assert(kStages % PL == 0, "each stage is always consumed by the same page lane");
+  static_assert(PL * NTW * Sm::kMergeFloats * 4 <= kStages * Gm::kStageBytes,
+                "merge buffers fit in the stage ring");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem + Sm::kStagesOff;
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem + Sm::kQOff);
+  int* lim = reinterpret_cast<int*>(smem + Sm::kLimOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
+  uint64_t* empty = full + kStages;
+  int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOff);
+  int* members = reinterpret_cast<int*>(smem + Sm::kMemOff);
+  __shared__ int s_nmem;
+  __shared__ int s_bad;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = blockIdx.y;                 // kv head
+  const int G = p.G, T = p.T;
+
+  // ------------------------------------------------------------------ unit
+  int pg0, pg1, slot, nrows, vlen;
+  bool direct;
+  int b_single = 0;                          // per-sequence mode: the sequence
+  if constexpr (!GROUP) {
+    const int b = blockIdx.z;
+    const int L = p.context_lens[b];
+    const int pre = (p.seq_group != nullptr && p.seq_group[b] >= 0)
+                        ? p.group_prefix_blocks[p.seq_group[b]] : 0;
+    if (L < T || L > p.max_ctx || pre < 0 || pre > p.max_prefix_blocks ||
+        pre * kBlockSize > L) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_pa_err, kErrBounds);
+      return;
+    }
+    const int nblk = (L + kBlockSize - 1) / kBlockSize;
+    pg0 = pre + blockIdx.x * p.ppb;
+    if (pg0 >= nblk) return;                 // partition past this sequence's end
+    pg1 = min(pg0 + p.ppb, nblk);
+    const int npre = (pre + p.ppb - 1) / p.ppb;
+    const int nparts = npre + (nblk - pre + p.ppb - 1) / p.ppb;
+    slot = npre + blockIdx.x;
+    direct = (pre == 0 && nparts == 1);
+    nrows = G * T;
+    vlen = L;
+    b_single = b;
+  } else {
+    const int gi = blockIdx.z / p.num_chunks;
+    const int chunk = blockIdx.z % p.num_chunks;
+    const int pre = p.group_prefix_blocks[gi];
+    if (pre < 0 || pre > p.max_prefix_blocks) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(&g_pa_err, kErrBounds);
+      return;
+    }
+    pg0 = blockIdx.x * p.ppb;
+    if (pg0 >= pre) return;
+    pg1 = min(pg0 + p.ppb, pre);
+    slot = blockIdx.x;
+    direct = false;
+    vlen = 0x7fffffff;                       // prefix pages are full blocks
+    const int mc = p.members_per_chunk;
+    if (warp == 0) {
+      // Members of group gi in ascending sequence order; keep ranks
+      // [chunk*mc, chunk*mc + mc).
+      int cnt = 0, bad = 0;
+      for (int base = 0; base < p.num_seqs; base += 32) {
+        const int b = base + lane;
+        const bool is = b < p.num_seqs && p.seq_group[b] == gi;
+        const unsigned bal = __ballot_sync(0xffffffffu, is);
+        if (is) {
+          const int r = cnt + __popc(bal & ((1u << lane) - 1)) - chunk * mc;
+          if (r >= 0 && r < mc) {
+            members[r] = b;
+            const int L = p.context_lens[b];
+            if (L < T || L > p.max_ctx || L < pre * kBlockSize) bad = 1;
+          }
+        }
+        cnt += __popc(bal);
+      }
+      bad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) {
+        s_nmem = max(0, min(mc, cnt - chunk * mc));
+        s_bad = bad;
+        if (bad && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(&g_pa_err, kErrBounds);
+      }
+    }
+    __syncthreads();
+    if (s_bad || s_nmem == 0) return;
+    nrows = s_nmem * G * T;
+  }
+
+  // ------------------------------------------------------------------ setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NTW);
+    }
+    fence_barrier_init();
+  }
+  if (warp == NCW && lane == 0) {
+    tma_prefetch_map(&tmk);
+    tma_prefetch_map(&tmv);
+  }
+  if (warp < NCW) {
+    // Gather the query rows of this unit into smem (zero rows pad to 8*NTW).
+    constexpr int CH = D / 8;                 // 16-byte chunks per row
+    for (int idx = threadIdx.x; idx < Sm::kRows * CH; idx += NCT) {
+      const int n = idx / CH, ch = idx % CH;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (n < nrows) {
+        const int m = n / (G * T), t = (n / G) % T, hl = n % G;
+        const int b = GROUP ? members[m] : b_single;
+        const size_t row = (static_cast<size_t>(b) * T + t) * p.Hq + g * G + hl;
+        v = reinterpret_cast<const uint4*>(p.q)[row * CH + ch];
+      }
+      *reinterpret_cast<uint4*>(qs + n * Gm::kQStride + ch * 8) = v;
+    }
+    for (int n = threadIdx.x; n < Sm::kRows; n += NCT) {
+      int lm = -1;                            // padding rows see nothing
+      if (n < nrows) {
+        const int m = n / (G * T), t = (n / G) % T;
+        lm = p.context_lens[GROUP ? members[m] : b_single] - T + t;
+      }
+      lim[n] = lm;
+    }
+  }
+  __syncthreads();
+
+  const int npages = pg1 - pg0;
+
+  // ------------------------------------------------------------------ producer
+  if (warp == NCW) {
+    const int32_t* trow =
+        p.block_tables + static_cast<size_t>(GROUP ? members[0] : b_single) * p.mbs;
+    bool aborted = false;
+    for (int base = 0; base < npages; base += 32) {
+      const int phys_l = (base + lane < npages) ? __ldg(trow + pg0 + base + lane) : 0;
+      const int cnt = min(32, npages - base);
+      for (int j = 0; j < cnt; ++j) {
+        const int phys = __shfl_sync(0xffffffffu, phys_l, j);
+        if (lane == 0) {
+          const int it = base + j;
+          const int s = it % kStages;
+          const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+          if (!aborted && !mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns)) aborted = true;
+          const bool ok = static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
+          if (!ok) atomicOr(&g_pa_err, kErrBounds);
+          if (!ok || aborted) {
+            stage_ok[s] = 0;
+            mbar_arrive(&full[s]);
+          } else {
+            stage_ok[s] = 1;
+            mbar_arrive_expect_tx(&full[s], Gm::kStageBytes);
+            const int row = (phys * p.Hkv + g) * kBlockSize;
+            uint8_t* st = stages + s * Gm::kStageBytes;
+#pragma unroll
+            for (int h = 0; h < Gm::kHalves; ++h)
+              tma_load_2d(st + h * Gm::kHalfBytes, &tmk, &full[s], h * 64, row);
+#pragma unroll
+            for (int h = 0; h < Gm::kHalves; ++h)
+              tma_load_2d(st + Gm::kPageBytes + h * Gm::kHalfBytes, &tmv, &full[s], h * 64, row);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // Do not leave while copies issued by this warp may still be landing.
+    if (lane == 0) {
+      for (int it = max(0, npages - kStages); it < npages; ++it)
+        mbar_wait(&full[it % kStages], static_cast<uint32_t>(it / kStages) & 1u, p.timeout_ns);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int col = warp % NTW;                // n-tile: rows 8*col .. 8*col+7
+  const int pl = warp / NTW;                 // page lane: pages pl, pl+PL, ...
+  const int gid = lane >> 2, q4 = lane & 3;
+  const int n0 = 8 * col + 2 * q4;           // this lane's two rows: n0, n0+1
+  const int lim0 = lim[n0], lim1 = lim[n0 + 1];
+  const float sl2 = p.scale_log2;
+
+  uint32_t qf[Gm::kKSteps][2];
+  {
+    const uint32_t qbase = smem_u32(qs) +
+                           static_cast<uint32_t>((8 * col + (lane & 7)) * Gm::kQStride * 2);
+#pragma unroll
+    for (int ks = 0; ks < Gm::kKSteps; ks += 2)
+      ldsm_x4(qf[ks][0], qf[ks][1], qf[ks + 1][0], qf[ks + 1][1],
+              qbase + static_cast<uint32_t>((2 * ks + (lane >> 3)) * 16));
+  }
+
+  float acc[Gm::kKSteps][4];
+#pragma unroll
+  for (int i = 0; i < Gm::kKSteps; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  bool aborted = false;
+
+  // per-lane ldmatrix row/chunk selectors
+  const int mi = lane >> 3, rr = lane & 7;
+  const int ktok = rr + ((mi & 1) << 3), kch = mi >> 1;     // K: A operand (tokens x dims)
+  const int vtok = rr + ((mi >> 1) << 3), vch = mi & 1;     // V: A operand (dims x tokens)
+
+  for (int it = pl; it < npages; it += PL) {
+    const int s = it % kStages;
+    const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+    if (!aborted && !mbar_wait(&full[s], ph, p.timeout_ns)) aborted = true;
+    if (!aborted && stage_ok[s]) {
+      const uint32_t kb = smem_u32(stages + s * Gm::kStageBytes);
+      const uint32_t vb = kb + Gm::kPageBytes;
+      const int tok0 = (pg0 + it) * kBlockSize;
+
+      // S^T[16 tokens x 8 rows] = K_page . Q^T  (two accumulation chains)
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < Gm::kKSteps; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(a0, a1, a2, a3, kb + page_off(ktok, 2 * ks + kch));
+        if (ks & 1)
+          mma_bf16_16816(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        else
+          mma_bf16_16816(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
+      // lane holds S^T[j0][n0], S^T[j0][n0+1], S^T[j0+8][n0], S^T[j0+8][n0+1]
+      const int j0 = tok0 + gid, j1 = j0 + 8;
+      const float t0 = (j0 <= lim0) ? (sa[0] + sb[0]) * sl2 : -CUDART_INF_F;
+      const float t1 = (j0 <= lim1) ? (sa[1] + sb[1]) * sl2 : -CUDART_INF_F;
+      const float t2 = (j1 <= lim0) ? (sa[2] + sb[2]) * sl2 : -CUDART_INF_F;
+      const float t3 = (j1 <= lim1) ? (sa[3] + sb[3]) * sl2 : -CUDART_INF_F;
+
+      // online softmax (log2 domain), statistics per row n0 / n0+1
+      float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
+      const float mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
+      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+      const float p0 = exp2f(t0 - mu0), p1 = exp2f(t1 - mu1);
+      const float p2 = exp2f(t2 - mu0), p3 = exp2f(t3 - mu1);
+      l0 = l0 * al0 + (p0 + p2);
+      l1 = l1 * al1 + (p1 + p3);
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
+
+      // P^T as B operands: bf16 high part and bf16 residual, transposed 8x8 blocks
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+      const float2 f01 = __bfloat1622float2(h01);
+      const float2 f23 = __bfloat1622float2(h23);
+      const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+      const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+      const uint32_t bh0 = movmatrix_trans(bf162_bits(h01));
+      const uint32_t bh1 = movmatrix_trans(bf162_bits(h23));
+      const uint32_t bl0 = movmatrix_trans(bf162_bits(r01));
+      const uint32_t bl1 = movmatrix_trans(bf162_bits(r23));
+
+      // V rows at or past the context end may hold anything (even NaN): their
+      // weight is 0, but 0 * NaN is NaN, so zero them in the operand.
+      const int nvalid = vlen - tok0;
+      uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+      if (nvalid < kBlockSize) {
+        mlo = (2 * q4 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < nvalid ? 0xffff0000u : 0u);
+        mhi = (2 * q4 + 8 < nvalid ? 0x0000ffffu : 0u) |
+              (2 * q4 + 9 < nvalid ? 0xffff0000u : 0u);
+      }
+      // O^T[D x 8] += V_page^T . P^T
+#pragma unroll
+      for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(a0, a1, a2, a3, vb + page_off(vtok, 2 * mt + vch));
+        a0 &= mlo;
+        a1 &= mlo;
+        a2 &= mhi;
+        a3 &= mhi;
+        mma_bf16_16816(acc[mt], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16_16816(acc[mt], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ------------------------------------------------------------------ merge + write
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  named_bar_sync(1, NCT);                    // every page consumed: stage ring is free
+  float* mbuf = reinterpret_cast<float*>(stages) + (pl * NTW + col) * Sm::kMergeFloats;
+  {
+    float* ob = mbuf + 16;
+    if (gid == 0) {
+      mbuf[2 * q4] = m0;
+      mbuf[2 * q4 + 1] = m1;
+      mbuf[8 + 2 * q4] = l0;
+      mbuf[8 + 2 * q4 + 1] = l1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+      ob[(2 * q4) * Gm::kOStride + 16 * mt + gid] = acc[mt][0];
+      ob[(2 * q4 + 1) * Gm::kOStride + 16 * mt + gid] = acc[mt][1];
+      ob[(2 * q4) * Gm::kOStride + 16 * mt + gid + 8] = acc[mt][2];
+      ob[(2 * q4 + 1) * Gm::kOStride + 16 * mt + gid + 8] = acc[mt][3];
+    }
+  }
+  named_bar_sync(1, NCT);
+
+  const float* mb0 = reinterpret_cast<const float*>(stages);
+  for (int idx = threadIdx.x; idx < nrows * (D / 2); idx += NCT) {
+    const int n = idx / (D / 2);
+    const int d = (idx % (D / 2)) * 2;
+    const int c = n >> 3, nn = n & 7;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int q = 0; q < PL; ++q) M = fmaxf(M, mb0[(q * NTW + c) * Sm::kMergeFloats + nn]);
+    float Ls = 0.f, o0 = 0.f, o1 = 0.f;
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int q = 0; q < PL; ++q) {
+        const float* mbq = mb0 + (q * NTW + c) * Sm::kMergeFloats;
+        const float f = exp2f(mbq[nn] - M);
+        Ls += f * mbq[8 + nn];
+        o0 += f * mbq[16 + nn * Gm::kOStride + d];
+        o1 += f * mbq[16 + nn * Gm::kOStride + d + 1];
+      }
+    }
+    const int m = n / (G * T), t = (n / G) % T, hl = n % G;
+    const int b = GROUP ? members[m] : b_single;
+    const size_t orow = (static_cast<size_t>(b) * T + t) * p.Hq + g * G + hl;
+    if (direct) {
+      const float inv = 1.f / Ls;
+      reinterpret_cast<__nv_bfloat162*>(p.out)[(orow * D + d) >> 1] =
+          __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    } else {
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const size_t pidx = orow * p.max_parts + slot;
+      reinterpret_cast<float2*>(p.part_o)[(pidx * D + d) >> 1] = make_float2(o0 * inv, o1 * inv);
+      if (d == 0) {
+        p.part_m[pidx] = M;
+        p.part_l[pidx] = Ls;
+      }
+    }
+  }
+}
+
+template <int D, int NTW, bool GROUP>
+cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                       dim3 grid, cudaStream_t s) {
+  constexpr int threads = (NTW * page_lanes_for(NTW) + 1) * 32;
+  constexpr int smem = Smem<D, NTW>::kAlloc;
+  auto kern = paged_attn_kernel<D, NTW, GROUP>;
+  static int configured_device = -1;         // attribute set once per device in practice
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  kern<<<grid, threads, smem, s>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool GROUP>
+cudaError_t launch_dispatch(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                            int ntw, dim3 grid, cudaStream_t s) {
+  switch (ntw) {
+    case 1: return launch_one<D, 1, GROUP>(tk, tv, p, grid, s);
+    case 2: return launch_one<D, 2, GROUP>(tk, tv, p, grid, s);
+    case 3: return launch_one<D, 3, GROUP>(tk, tv, p, grid, s);
+    case 4: return launch_one<D, 4, GROUP>(tk, tv, p, grid, s);
+    case 5: return launch_one<D, 5, GROUP>(tk, tv, p, grid, s);
+    case 6: return launch_one<D, 6, GROUP>(tk, tv, p, grid, s);
+    case 7: return launch_one<D, 7, GROUP>(tk, tv, p, grid, s);
+    case 8: return launch_one<D, 8, GROUP>(tk, tv, p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+inline cudaError_t take_error_word(unsigned* bits) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_pa_err, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_pa_err, &zero, sizeof(zero));
+  *bits |= v;
+  return e;
+}
+
+}  // namespace pa

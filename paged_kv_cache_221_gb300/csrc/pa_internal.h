@@ -1,0 +1,67 @@
+// Internal host/device interface between the C ABI (pa_api.cpp) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Bits of the sticky device error word (one word per kernel translation unit).
+enum : unsigned { kErrBounds = 1u, kErrTimeout = 2u };
+
+constexpr int kBlockSize = 16;        // tokens per physical block (the only size built)
+constexpr int kStages = 8;            // pages in flight per CTA (multiple of every PL)
+constexpr int kMaxRows = 64;          // query rows per CTA (8 n-tiles of 8)
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
+
+// Everything an attention launch needs besides the two tensor maps.
+struct AttnParams {
+  const void* q;                  // bf16 [B, T, Hq, D]
+  void* out;                      // bf16 [B, T, Hq, D]
+  const int32_t* block_tables;    // [B, mbs]
+  const int32_t* context_lens;    // [B]
+  float* part_o;                  // [B*T*Hq, max_parts, D]   (split-KV partials)
+  float* part_m;                  // [B*T*Hq, max_parts]      running max, log2 domain
+  float* part_l;                  // [B*T*Hq, max_parts]      softmax denominator
+  const int32_t* seq_group;       // [B] or nullptr
+  const int32_t* group_prefix_blocks;  // [num_groups] or nullptr
+  int mbs;                        // max_blocks_per_seq
+  int max_ctx;                    // bound on context_lens
+  int num_seqs, T, Hq, Hkv, G, num_blocks;
+  int ppb;                        // pages (blocks) per partition
+  int max_parts;                  // partition slots per query row
+  int members_per_chunk;          // shared-prefix kernel: group members per CTA
+  int num_chunks;                 // shared-prefix kernel: CTAs per group (per partition, head)
+  int max_prefix_blocks;          // bound on group_prefix_blocks (launch sizing)
+  float scale_log2;               // softmax scale * log2(e)
+  unsigned long long timeout_ns;  // limit of every pipeline wait
+};
+
+// Consumer-warp layout of the attention kernel for `ntw` n-tiles of 8 rows.
+__host__ __device__ constexpr int page_lanes_for(int ntw) { return ntw == 1 ? 4 : (ntw <= 4 ? 2 : 1); }
+
+// Kernel launchers (one translation unit per head_dim and mode).
+cudaError_t launch_attn_d64(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                            int ntw, bool group, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                             int ntw, bool group, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_group_d64(const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const AttnParams& p, int ntw, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_group_d128(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const AttnParams& p, int ntw, dim3 grid, cudaStream_t s);
+cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s);
+cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, void* v_cache,
+                           const int64_t* slots, int num_tokens, int num_blocks, int hkv,
+                           int head_dim, int block_size, cudaStream_t s);
+cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
+
+// Read and clear the device error word of each translation unit (synchronous).
+cudaError_t take_error_attn_d64(unsigned* bits);
+cudaError_t take_error_attn_d128(unsigned* bits);
+cudaError_t take_error_group_d64(unsigned* bits);
+cudaError_t take_error_group_d128(unsigned* bits);
+cudaError_t take_error_misc(unsigned* bits);
+
+}  // namespace pa
