@@ -183,6 +183,36 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
                                   void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_static_scratch — pa_decode without caller-provided scratch, for
+ * callers that may not allocate device memory: a plugin that its host runtime
+ * gives only input and output buffers, or a server that reserves all device
+ * memory at start-up and must not call cudaMalloc/cudaFree afterwards.  The
+ * paper has no counterpart; this is a library convenience.
+ *
+ * The split-KV scratch comes from one fixed array of 32 MiB (33554432 bytes)
+ * inside this library's device image.  It exists on every GPU the library is
+ * loaded on and is held until the process exits.  If the call needs more than
+ * 32 MiB (pa_workspace_size with the same sizes, num_query_tokens 1,
+ * max_prefix_blocks 0) it returns PA_ERR_WORKSPACE and launches nothing.
+ * Nothing is allocated by this call or by anything it calls.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls in the process share the one array
+ * and it keeps what the last call wrote; nothing in it needs to start at zero
+ * (every partial is written before it is read).  Calls whose executions
+ * overlap on the GPU (e.g. on two streams) race on the array: serialise them.
+ * Arguments, results and errors are otherwise those of pa_decode.
+ */
+pa_status pa_decode_static_scratch(void* out, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int max_context_len, int num_seqs, int num_blocks,
+                                   int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, int partition_size,
+                                   pa_stream_t stream);
+
+/*
  * pa_get_device_error — synchronise `stream`, then return and clear the sticky
  * device error word: PA_ERR_TIMEOUT if any pipeline wait gave up, else
  * PA_ERR_BOUNDS if any out-of-range id, slot or length was seen, else PA_OK

@@ -31,6 +31,8 @@ SIGNATURES = {
                        _i, _vp, _sz, _vp]),
     "pa_decode_shared_prefix": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                      _i, _f, _i, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+    "pa_decode_static_scratch": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
+                                      _i, _i, _f, _i, _vp]),
     "pa_get_device_error": (_i, [_vp]),
     "pa_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
 }
