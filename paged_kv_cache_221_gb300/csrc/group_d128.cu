@@ -5,8 +5,8 @@
 namespace pa {
 
 cudaError_t launch_attn_group_d128(const CUtensorMap& tk, const CUtensorMap& tv,
-                                  const AttnParams& p, int ntw, dim3 grid, cudaStream_t s) {
-  return launch_dispatch<128, true>(tk, tv, p, ntw, grid, s);
+                                  const AttnParams& p, int rows, dim3 grid, cudaStream_t s) {
+  return launch_dispatch<128, true>(tk, tv, p, rows, grid, s);
 }
 
 cudaError_t take_error_group_d128(unsigned* bits) { return take_error_word(bits); }

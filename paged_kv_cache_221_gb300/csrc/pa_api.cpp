@@ -7,7 +7,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "../../include/paged_attn.h"
+#include "paged_attn.h"
 #include "pa_internal.h"
 
 using namespace pa;
@@ -55,8 +55,10 @@ struct Plan {
   size_t off_m = 0, off_l = 0;
 };
 
+// 1024-token partitions (64 pages per CTA) measured best on GB300 for contexts of
+// 512 .. 32768 tokens; shorter contexts stay whole.
 int default_partition_tokens(int max_context_len) {
-  return max_context_len > 512 ? 512 : ceil_div(max_context_len, kBlockSize) * kBlockSize;
+  return max_context_len > 1024 ? 1024 : ceil_div(max_context_len, kBlockSize) * kBlockSize;
 }
 
 Plan make_plan(int num_seqs, int hq, int T, int max_ctx, int head_dim, int partition_size,
@@ -184,17 +186,17 @@ pa_status run_attention(const AttnArgs& a) {
     p.num_chunks = ceil_div(a.max_group_size, mc);
     const long long gz = static_cast<long long>(a.num_groups) * p.num_chunks;
     if (gz > 65535) return PA_ERR_UNSUPPORTED;
-    const int ntw = ceil_div(static_cast<long long>(mc) * G * a.T, 8);
+    const int rows = mc * G * a.T;
     dim3 grid(ceil_div(a.max_prefix_blocks, plan.ppb), a.hkv, static_cast<unsigned>(gz));
-    e = a.head_dim == 64 ? launch_attn_group_d64(tk, tv, p, ntw, grid, a.stream)
-                         : launch_attn_group_d128(tk, tv, p, ntw, grid, a.stream);
+    e = a.head_dim == 64 ? launch_attn_group_d64(tk, tv, p, rows, grid, a.stream)
+                         : launch_attn_group_d128(tk, tv, p, rows, grid, a.stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   {
-    const int ntw = ceil_div(static_cast<long long>(G) * a.T, 8);
+    const int rows = G * a.T;
     dim3 grid(ceil_div(max_blocks, plan.ppb), a.hkv, a.num_seqs);
-    e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, ntw, false, grid, a.stream)
-                         : launch_attn_d128(tk, tv, p, ntw, false, grid, a.stream);
+    e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream)
+                         : launch_attn_d128(tk, tv, p, rows, grid, a.stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (plan.ws_bytes > 0) {

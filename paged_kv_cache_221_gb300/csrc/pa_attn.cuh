@@ -17,7 +17,9 @@
 // (S^T[16 tokens x 8 rows] = K_page[16 x D] . Q^T[D x 8]) and head dims are the
 // M dimension of the output tile (O^T[D x 8] += V_page^T[D x 16] . P^T[16 x 8]),
 // so a 16-token page is exactly one m16n8k16 step and the query rows of the
-// CTA (1 .. 64) fill the N = 8 side, one n-tile per consumer-warp column.
+// CTA (1 .. 64) fill the N side in n-tiles of 8.  A consumer warp carries NT
+// n-tiles, so it reads each K/V page from shared memory once for up to 32 rows;
+// NTW warp columns split larger row sets, and PL page lanes split the pages.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -39,9 +41,18 @@ struct Geo {
   static constexpr int kKSteps = D / 16;
 };
 
-template <int D, int NTW>
+// Consumer-warp layout: NT n-tiles of 8 query rows per warp, NTW warp columns
+// (rows 8*NT*NTW per CTA), PL page lanes (warps of one column that split the
+// pages), and the CTAs per SM the register budget must allow.
+template <int NT_, int NTW_, int PL_, int MINB_>
+struct Cfg {
+  static constexpr int NT = NT_, NTW = NTW_, PL = PL_, MINB = MINB_;
+  static constexpr int kThreads = (NTW * PL + 1) * 32;
+};
+
+template <int D, int NT, int NTW>
 struct Smem {
-  static constexpr int kRows = 8 * NTW;
+  static constexpr int kRows = 8 * NT * NTW;
   static constexpr int kStagesOff = 0;
   static constexpr int kQOff = kStages * Geo<D>::kStageBytes;
   static constexpr int kLimOff = kQOff + kRows * Geo<D>::kQStride * 2;
@@ -50,8 +61,9 @@ struct Smem {
   static constexpr int kMemOff = kOkOff + kStages * 4;
   static constexpr int kBytes = kMemOff + kMaxRows * 4;
   static constexpr int kAlloc = kBytes + 1024;          // room to align the base to 1 KB
-  // merge buffers (reuse the stage ring once every page is consumed)
-  static constexpr int kMergeFloats = 16 + 8 * Geo<D>::kOStride;
+  // merge buffer of one (page lane, warp column): m[8NT], l[8NT], O[8NT][kOStride]
+  // (reuses the stage ring once every page is consumed)
+  static constexpr int kMergeFloats = 16 * NT + 8 * NT * Geo<D>::kOStride;
 };
 
 // Byte offset of 16-byte chunk `ch` (of D/8) of token row `tok` inside one
@@ -62,15 +74,15 @@ __device__ __forceinline__ uint32_t page_off(int tok, int ch) {
                                (((ch & 7) ^ (tok & 7)) << 4));
 }
 
-template <int D, int NTW, bool GROUP>
-__global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
+template <int D, class C, bool GROUP>
+__global__ void __launch_bounds__(C::kThreads, C::MINB)
     paged_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
-  constexpr int PL = page_lanes_for(NTW);
+  constexpr int NT = C::NT, NTW = C::NTW, PL = C::PL;
   constexpr int NCW = NTW * PL;              // consumer warps
   constexpr int NCT = NCW * 32;              // consumer threads
   using Gm = Geo<D>;
-  using Sm = Smem<D, NTW>;
+  using Sm = Smem<D, NT, NTW>;
   static_assert(kStages % PL == 0, "each stage is always consumed by the same page lane");
   static_assert(PL * NTW * Sm::kMergeFloats * 4 <= kStages * Gm::kStageBytes,
                 "merge buffers fit in the stage ring");
@@ -164,6 +176,17 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
   }
 
   // ------------------------------------------------------------------ setup
+  const int npages = pg1 - pg0;
+  const int32_t* trow =
+      p.block_tables + static_cast<size_t>(GROUP ? members[0] : b_single) * p.mbs;
+  int phys_first = 0;                        // first 32 block ids, loaded before the sync
+  if (warp == NCW) {
+    if (lane < npages) phys_first = __ldg(trow + pg0 + lane);
+    if (lane == 0) {
+      tma_prefetch_map(&tmk);
+      tma_prefetch_map(&tmv);
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -171,44 +194,15 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
     }
     fence_barrier_init();
   }
-  if (warp == NCW && lane == 0) {
-    tma_prefetch_map(&tmk);
-    tma_prefetch_map(&tmv);
-  }
-  if (warp < NCW) {
-    // Gather the query rows of this unit into smem (zero rows pad to 8*NTW).
-    constexpr int CH = D / 8;                 // 16-byte chunks per row
-    for (int idx = threadIdx.x; idx < Sm::kRows * CH; idx += NCT) {
-      const int n = idx / CH, ch = idx % CH;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (n < nrows) {
-        const int m = n / (G * T), t = (n / G) % T, hl = n % G;
-        const int b = GROUP ? members[m] : b_single;
-        const size_t row = (static_cast<size_t>(b) * T + t) * p.Hq + g * G + hl;
-        v = reinterpret_cast<const uint4*>(p.q)[row * CH + ch];
-      }
-      *reinterpret_cast<uint4*>(qs + n * Gm::kQStride + ch * 8) = v;
-    }
-    for (int n = threadIdx.x; n < Sm::kRows; n += NCT) {
-      int lm = -1;                            // padding rows see nothing
-      if (n < nrows) {
-        const int m = n / (G * T), t = (n / G) % T;
-        lm = p.context_lens[GROUP ? members[m] : b_single] - T + t;
-      }
-      lim[n] = lm;
-    }
-  }
-  __syncthreads();
-
-  const int npages = pg1 - pg0;
+  __syncthreads();                           // barriers initialised before anyone uses them
 
   // ------------------------------------------------------------------ producer
+  // Starts streaming pages at once; the consumers gather the query rows meanwhile.
   if (warp == NCW) {
-    const int32_t* trow =
-        p.block_tables + static_cast<size_t>(GROUP ? members[0] : b_single) * p.mbs;
     bool aborted = false;
     for (int base = 0; base < npages; base += 32) {
-      const int phys_l = (base + lane < npages) ? __ldg(trow + pg0 + base + lane) : 0;
+      const int phys_l = base == 0 ? phys_first
+                                   : ((base + lane < npages) ? __ldg(trow + pg0 + base + lane) : 0);
       const int cnt = min(32, npages - base);
       for (int j = 0; j < cnt; ++j) {
         const int phys = __shfl_sync(0xffffffffu, phys_l, j);
@@ -246,28 +240,69 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
     return;
   }
 
-  // ------------------------------------------------------------------ consumers
-  const int col = warp % NTW;                // n-tile: rows 8*col .. 8*col+7
-  const int pl = warp / NTW;                 // page lane: pages pl, pl+PL, ...
-  const int gid = lane >> 2, q4 = lane & 3;
-  const int n0 = 8 * col + 2 * q4;           // this lane's two rows: n0, n0+1
-  const int lim0 = lim[n0], lim1 = lim[n0 + 1];
-  const float sl2 = p.scale_log2;
-
-  uint32_t qf[Gm::kKSteps][2];
+  // ------------------------------------------------------------------ query rows
   {
-    const uint32_t qbase = smem_u32(qs) +
-                           static_cast<uint32_t>((8 * col + (lane & 7)) * Gm::kQStride * 2);
-#pragma unroll
-    for (int ks = 0; ks < Gm::kKSteps; ks += 2)
-      ldsm_x4(qf[ks][0], qf[ks][1], qf[ks + 1][0], qf[ks + 1][1],
-              qbase + static_cast<uint32_t>((2 * ks + (lane >> 3)) * 16));
+    // Gather the query rows of this unit into smem (zero rows pad to 8*NTW).
+    constexpr int CH = D / 8;                 // 16-byte chunks per row
+    for (int idx = threadIdx.x; idx < Sm::kRows * CH; idx += NCT) {
+      const int n = idx / CH, ch = idx % CH;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (n < nrows) {
+        const int m = n / (G * T), t = (n / G) % T, hl = n % G;
+        const int b = GROUP ? members[m] : b_single;
+        const size_t row = (static_cast<size_t>(b) * T + t) * p.Hq + g * G + hl;
+        v = reinterpret_cast<const uint4*>(p.q)[row * CH + ch];
+      }
+      *reinterpret_cast<uint4*>(qs + n * Gm::kQStride + ch * 8) = v;
+    }
+    for (int n = threadIdx.x; n < Sm::kRows; n += NCT) {
+      int lm = -1;                            // padding rows see nothing
+      if (n < nrows) {
+        const int m = n / (G * T), t = (n / G) % T;
+        lm = p.context_lens[GROUP ? members[m] : b_single] - T + t;
+      }
+      lim[n] = lm;
+    }
+    named_bar_sync(1, NCT);
   }
 
-  float acc[Gm::kKSteps][4];
+  // ------------------------------------------------------------------ consumers
+  const int col = warp % NTW;                // rows 8*NT*col .. 8*NT*(col+1)-1
+  const int pl = warp / NTW;                 // page lane: pages pl, pl+PL, ...
+  const int gid = lane >> 2, q4 = lane & 3;
+  const int rbase = 8 * NT * col;
+  const float sl2 = p.scale_log2;
+  int lim0[NT], lim1[NT];                    // this lane's rows rbase+8j+2q4 (+1)
 #pragma unroll
-  for (int i = 0; i < Gm::kKSteps; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  for (int j = 0; j < NT; ++j) {
+    lim0[j] = lim[rbase + 8 * j + 2 * q4];
+    lim1[j] = lim[rbase + 8 * j + 2 * q4 + 1];
+  }
+  // Q^T B operands: held in registers for NT <= 2, re-read from smem per page otherwise.
+  constexpr bool kQRegs = NT <= 2;
+  const uint32_t qrow = smem_u32(qs) +
+                        static_cast<uint32_t>((rbase + (lane & 7)) * Gm::kQStride * 2 +
+                                              (lane >> 3) * 16);
+  uint32_t qf[kQRegs ? NT : 1][kQRegs ? Gm::kKSteps : 1][2];
+  if constexpr (kQRegs) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int ks = 0; ks < Gm::kKSteps; ks += 2)
+        ldsm_x4(qf[j][ks][0], qf[j][ks][1], qf[j][ks + 1][0], qf[j][ks + 1][1],
+                qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + ks * 32));
+  }
+
+  float acc[NT][Gm::kKSteps][4];
+  float m0[NT], m1[NT], l0[NT], l1[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+#pragma unroll
+    for (int i = 0; i < Gm::kKSteps; ++i)
+      acc[j][i][0] = acc[j][i][1] = acc[j][i][2] = acc[j][i][3] = 0.f;
+    m0[j] = m1[j] = -CUDART_INF_F;
+    l0[j] = l1[j] = 0.f;
+  }
   bool aborted = false;
 
   // per-lane ldmatrix row/chunk selectors
@@ -284,60 +319,33 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
       const uint32_t vb = kb + Gm::kPageBytes;
       const int tok0 = (pg0 + it) * kBlockSize;
 
-      // S^T[16 tokens x 8 rows] = K_page . Q^T  (two accumulation chains)
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      // S^T[16 tokens x 8 rows] = K_page . Q^T per n-tile (two accumulation chains)
+      float sa[NT][4], sb[NT][4];
 #pragma unroll
-      for (int ks = 0; ks < Gm::kKSteps; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(a0, a1, a2, a3, kb + page_off(ktok, 2 * ks + kch));
-        if (ks & 1)
-          mma_bf16_16816(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-        else
-          mma_bf16_16816(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-      }
-      // lane holds S^T[j0][n0], S^T[j0][n0+1], S^T[j0+8][n0], S^T[j0+8][n0+1]
-      const int j0 = tok0 + gid, j1 = j0 + 8;
-      const float t0 = (j0 <= lim0) ? (sa[0] + sb[0]) * sl2 : -CUDART_INF_F;
-      const float t1 = (j0 <= lim1) ? (sa[1] + sb[1]) * sl2 : -CUDART_INF_F;
-      const float t2 = (j1 <= lim0) ? (sa[2] + sb[2]) * sl2 : -CUDART_INF_F;
-      const float t3 = (j1 <= lim1) ? (sa[3] + sb[3]) * sl2 : -CUDART_INF_F;
-
-      // online softmax (log2 domain), statistics per row n0 / n0+1
-      float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+      for (int j = 0; j < NT; ++j)
+        sa[j][0] = sa[j][1] = sa[j][2] = sa[j][3] = sb[j][0] = sb[j][1] = sb[j][2] =
+            sb[j][3] = 0.f;
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
-      const float mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
-      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-      const float p0 = exp2f(t0 - mu0), p1 = exp2f(t1 - mu1);
-      const float p2 = exp2f(t2 - mu0), p3 = exp2f(t3 - mu1);
-      l0 = l0 * al0 + (p0 + p2);
-      l1 = l1 * al1 + (p1 + p3);
-      m0 = mn0;
-      m1 = mn1;
+      for (int k2 = 0; k2 < Gm::kKSteps; k2 += 2) {
+        uint32_t a[2][4];
+        ldsm_x4(a[0][0], a[0][1], a[0][2], a[0][3], kb + page_off(ktok, 2 * k2 + kch));
+        ldsm_x4(a[1][0], a[1][1], a[1][2], a[1][3], kb + page_off(ktok, 2 * k2 + 2 + kch));
 #pragma unroll
-      for (int mt = 0; mt < Gm::kKSteps; ++mt) {
-        acc[mt][0] *= al0;
-        acc[mt][1] *= al1;
-        acc[mt][2] *= al0;
-        acc[mt][3] *= al1;
+        for (int j = 0; j < NT; ++j) {
+          uint32_t b00, b01, b10, b11;
+          if constexpr (kQRegs) {
+            b00 = qf[j][k2][0];
+            b01 = qf[j][k2][1];
+            b10 = qf[j][k2 + 1][0];
+            b11 = qf[j][k2 + 1][1];
+          } else {
+            ldsm_x4(b00, b01, b10, b11,
+                    qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + k2 * 32));
+          }
+          mma_bf16_16816(sa[j], a[0][0], a[0][1], a[0][2], a[0][3], b00, b01);
+          mma_bf16_16816(sb[j], a[1][0], a[1][1], a[1][2], a[1][3], b10, b11);
+        }
       }
-
-      // P^T as B operands: bf16 high part and bf16 residual, transposed 8x8 blocks
-      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
-      const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
-      const float2 f01 = __bfloat1622float2(h01);
-      const float2 f23 = __bfloat1622float2(h23);
-      const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
-      const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
-      const uint32_t bh0 = movmatrix_trans(bf162_bits(h01));
-      const uint32_t bh1 = movmatrix_trans(bf162_bits(h23));
-      const uint32_t bl0 = movmatrix_trans(bf162_bits(r01));
-      const uint32_t bl1 = movmatrix_trans(bf162_bits(r23));
 
       // V rows at or past the context end may hold anything (even NaN): their
       // weight is 0, but 0 * NaN is NaN, so zero them in the operand.
@@ -348,7 +356,63 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
         mhi = (2 * q4 + 8 < nvalid ? 0x0000ffffu : 0u) |
               (2 * q4 + 9 < nvalid ? 0xffff0000u : 0u);
       }
-      // O^T[D x 8] += V_page^T . P^T
+
+      uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
+      const int j0 = tok0 + gid, j1 = j0 + 8;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        // lane holds S^T[j0][n], S^T[j0][n+1], S^T[j0+8][n], S^T[j0+8][n+1], n = rbase+8j+2q4
+        const float t0 = (j0 <= lim0[j]) ? (sa[j][0] + sb[j][0]) * sl2 : -CUDART_INF_F;
+        const float t1 = (j0 <= lim1[j]) ? (sa[j][1] + sb[j][1]) * sl2 : -CUDART_INF_F;
+        const float t2 = (j1 <= lim0[j]) ? (sa[j][2] + sb[j][2]) * sl2 : -CUDART_INF_F;
+        const float t3 = (j1 <= lim1[j]) ? (sa[j][3] + sb[j][3]) * sl2 : -CUDART_INF_F;
+
+        // online softmax (log2 domain), statistics per row.  The reference max m
+        // only moves when a score exceeds it by more than 8 (so every weight
+        // 2^(t - m) stays <= 256); the accumulators are rescaled only then.
+        float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const bool up0 = mx0 > m0[j] + 8.f, up1 = mx1 > m1[j] + 8.f;
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+          const float al0 = up0 ? exp2f(m0[j] - mx0) : 1.f;
+          const float al1 = up1 ? exp2f(m1[j] - mx1) : 1.f;
+          if (up0) m0[j] = mx0;
+          if (up1) m1[j] = mx1;
+          l0[j] *= al0;
+          l1[j] *= al1;
+#pragma unroll
+          for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+            acc[j][mt][0] *= al0;
+            acc[j][mt][1] *= al1;
+            acc[j][mt][2] *= al0;
+            acc[j][mt][3] *= al1;
+          }
+        }
+        const float mu0 = (m0[j] == -CUDART_INF_F) ? 0.f : m0[j];
+        const float mu1 = (m1[j] == -CUDART_INF_F) ? 0.f : m1[j];
+        const float p0 = exp2f(t0 - mu0), p1 = exp2f(t1 - mu1);
+        const float p2 = exp2f(t2 - mu0), p3 = exp2f(t3 - mu1);
+        l0[j] += p0 + p2;
+        l1[j] += p1 + p3;
+
+        // P^T as B operands: bf16 high part and bf16 residual, transposed 8x8 blocks
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+        const float2 f01 = __bfloat1622float2(h01);
+        const float2 f23 = __bfloat1622float2(h23);
+        const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+        const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+        bh0[j] = movmatrix_trans(bf162_bits(h01));
+        bh1[j] = movmatrix_trans(bf162_bits(h23));
+        bl0[j] = movmatrix_trans(bf162_bits(r01));
+        bl1[j] = movmatrix_trans(bf162_bits(r23));
+      }
+
+      // O^T[D x 8] += V_page^T . P^T per n-tile
 #pragma unroll
       for (int mt = 0; mt < Gm::kKSteps; ++mt) {
         uint32_t a0, a1, a2, a3;
@@ -357,8 +421,11 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
         a1 &= mlo;
         a2 &= mhi;
         a3 &= mhi;
-        mma_bf16_16816(acc[mt], a0, a1, a2, a3, bh0, bh1);
-        mma_bf16_16816(acc[mt], a0, a1, a2, a3, bl0, bl1);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bh0[j], bh1[j]);
+          mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bl0[j], bl1[j]);
+        }
       }
     }
     __syncwarp();
@@ -367,26 +434,33 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
 
   // ------------------------------------------------------------------ merge + write
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  for (int j = 0; j < NT; ++j) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0[j] += __shfl_xor_sync(0xffffffffu, l0[j], o);
+      l1[j] += __shfl_xor_sync(0xffffffffu, l1[j], o);
+    }
   }
   named_bar_sync(1, NCT);                    // every page consumed: stage ring is free
-  float* mbuf = reinterpret_cast<float*>(stages) + (pl * NTW + col) * Sm::kMergeFloats;
   {
-    float* ob = mbuf + 16;
-    if (gid == 0) {
-      mbuf[2 * q4] = m0;
-      mbuf[2 * q4 + 1] = m1;
-      mbuf[8 + 2 * q4] = l0;
-      mbuf[8 + 2 * q4 + 1] = l1;
-    }
+    float* mbuf = reinterpret_cast<float*>(stages) + (pl * NTW + col) * Sm::kMergeFloats;
+    float* ob = mbuf + 16 * NT;
 #pragma unroll
-    for (int mt = 0; mt < Gm::kKSteps; ++mt) {
-      ob[(2 * q4) * Gm::kOStride + 16 * mt + gid] = acc[mt][0];
-      ob[(2 * q4 + 1) * Gm::kOStride + 16 * mt + gid] = acc[mt][1];
-      ob[(2 * q4) * Gm::kOStride + 16 * mt + gid + 8] = acc[mt][2];
-      ob[(2 * q4 + 1) * Gm::kOStride + 16 * mt + gid + 8] = acc[mt][3];
+    for (int j = 0; j < NT; ++j) {
+      const int r0 = 8 * j + 2 * q4;          // row within this warp's 8*NT rows
+      if (gid == 0) {
+        mbuf[r0] = m0[j];
+        mbuf[r0 + 1] = m1[j];
+        mbuf[8 * NT + r0] = l0[j];
+        mbuf[8 * NT + r0 + 1] = l1[j];
+      }
+#pragma unroll
+      for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+        ob[r0 * Gm::kOStride + 16 * mt + gid] = acc[j][mt][0];
+        ob[(r0 + 1) * Gm::kOStride + 16 * mt + gid] = acc[j][mt][1];
+        ob[r0 * Gm::kOStride + 16 * mt + gid + 8] = acc[j][mt][2];
+        ob[(r0 + 1) * Gm::kOStride + 16 * mt + gid + 8] = acc[j][mt][3];
+      }
     }
   }
   named_bar_sync(1, NCT);
@@ -395,7 +469,7 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
   for (int idx = threadIdx.x; idx < nrows * (D / 2); idx += NCT) {
     const int n = idx / (D / 2);
     const int d = (idx % (D / 2)) * 2;
-    const int c = n >> 3, nn = n & 7;
+    const int c = n / (8 * NT), nn = n % (8 * NT);
     float M = -CUDART_INF_F;
 #pragma unroll
     for (int q = 0; q < PL; ++q) M = fmaxf(M, mb0[(q * NTW + c) * Sm::kMergeFloats + nn]);
@@ -405,9 +479,9 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
       for (int q = 0; q < PL; ++q) {
         const float* mbq = mb0 + (q * NTW + c) * Sm::kMergeFloats;
         const float f = exp2f(mbq[nn] - M);
-        Ls += f * mbq[8 + nn];
-        o0 += f * mbq[16 + nn * Gm::kOStride + d];
-        o1 += f * mbq[16 + nn * Gm::kOStride + d + 1];
+        Ls += f * mbq[8 * NT + nn];
+        o0 += f * mbq[16 * NT + nn * Gm::kOStride + d];
+        o1 += f * mbq[16 * NT + nn * Gm::kOStride + d + 1];
       }
     }
     const int m = n / (G * T), t = (n / G) % T, hl = n % G;
@@ -429,12 +503,11 @@ __global__ void __launch_bounds__((NTW * page_lanes_for(NTW) + 1) * 32)
   }
 }
 
-template <int D, int NTW, bool GROUP>
+template <int D, class C, bool GROUP>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                        dim3 grid, cudaStream_t s) {
-  constexpr int threads = (NTW * page_lanes_for(NTW) + 1) * 32;
-  constexpr int smem = Smem<D, NTW>::kAlloc;
-  auto kern = paged_attn_kernel<D, NTW, GROUP>;
+  constexpr int smem = Smem<D, C::NT, C::NTW>::kAlloc;
+  auto kern = paged_attn_kernel<D, C, GROUP>;
   static int configured_device = -1;         // attribute set once per device in practice
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -444,24 +517,22 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const AttnP
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  kern<<<grid, threads, smem, s>>>(tk, tv, p);
+  kern<<<grid, C::kThreads, smem, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
+// `rows` = query rows per CTA (1..64).  One n-tile per warp keeps registers low
+// and many warps resident (latency hiding); warp columns split the rows.
 template <int D, bool GROUP>
 cudaError_t launch_dispatch(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                            int ntw, dim3 grid, cudaStream_t s) {
-  switch (ntw) {
-    case 1: return launch_one<D, 1, GROUP>(tk, tv, p, grid, s);
-    case 2: return launch_one<D, 2, GROUP>(tk, tv, p, grid, s);
-    case 3: return launch_one<D, 3, GROUP>(tk, tv, p, grid, s);
-    case 4: return launch_one<D, 4, GROUP>(tk, tv, p, grid, s);
-    case 5: return launch_one<D, 5, GROUP>(tk, tv, p, grid, s);
-    case 6: return launch_one<D, 6, GROUP>(tk, tv, p, grid, s);
-    case 7: return launch_one<D, 7, GROUP>(tk, tv, p, grid, s);
-    case 8: return launch_one<D, 8, GROUP>(tk, tv, p, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
+                            int rows, dim3 grid, cudaStream_t s) {
+  if (rows <= 0) return cudaErrorInvalidValue;
+  if (rows <= 8) return launch_one<D, Cfg<1, 1, 4, 3>, GROUP>(tk, tv, p, grid, s);
+  if (rows <= 16) return launch_one<D, Cfg<1, 2, 2, 3>, GROUP>(tk, tv, p, grid, s);
+  if (rows <= 24) return launch_one<D, Cfg<1, 3, 2, 3>, GROUP>(tk, tv, p, grid, s);
+  if (rows <= 32) return launch_one<D, Cfg<1, 4, 2, 2>, GROUP>(tk, tv, p, grid, s);
+  if (rows <= 64) return launch_one<D, Cfg<2, 4, 1, 2>, GROUP>(tk, tv, p, grid, s);
+  return cudaErrorInvalidValue;
 }
 
 inline cudaError_t take_error_word(unsigned* bits) {

@@ -39,18 +39,16 @@ struct AttnParams {
   unsigned long long timeout_ns;  // limit of every pipeline wait
 };
 
-// Consumer-warp layout of the attention kernel for `ntw` n-tiles of 8 rows.
-__host__ __device__ constexpr int page_lanes_for(int ntw) { return ntw == 1 ? 4 : (ntw <= 4 ? 2 : 1); }
-
-// Kernel launchers (one translation unit per head_dim and mode).
+// Kernel launchers (one translation unit per head_dim and mode); `rows` is the
+// number of query rows one CTA carries (1 .. kMaxRows).
 cudaError_t launch_attn_d64(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                            int ntw, bool group, dim3 grid, cudaStream_t s);
+                            int rows, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                             int ntw, bool group, dim3 grid, cudaStream_t s);
+                             int rows, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_group_d64(const CUtensorMap& tk, const CUtensorMap& tv,
-                                  const AttnParams& p, int ntw, dim3 grid, cudaStream_t s);
+                                  const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_group_d128(const CUtensorMap& tk, const CUtensorMap& tv,
-                                   const AttnParams& p, int ntw, dim3 grid, cudaStream_t s);
+                                   const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_blocks, int hkv,

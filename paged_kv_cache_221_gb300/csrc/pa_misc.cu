@@ -53,9 +53,15 @@ cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, vo
 // row holds O_i (normalised), m_i (running max, log2 domain) and l_i (sum of
 // 2^(s - m_i)); the merged row is sum_i w_i O_i / sum_i w_i, w_i = l_i 2^(m_i - M),
 // M = max_i m_i.  Rows whose sequence fit in one partition were written by the
-// attention kernel directly and are skipped here (same predicate).
+// attention kernel directly and are skipped here (same predicate).  The
+// statistics of up to kChunk partitions are loaded in parallel (one per
+// thread) and the partial rows are summed with independent loads in flight.
 template <int D>
 __global__ void __launch_bounds__(D) splitkv_reduce_kernel(const AttnParams p) {
+  constexpr int kChunk = D;
+  constexpr int kWarps = D / 32;
+  __shared__ float s_w[kChunk];
+  __shared__ float s_red[kWarps];
   const int orow = blockIdx.x;
   const int b = orow / (p.T * p.Hq);
   const int L = p.context_lens[b];
@@ -70,19 +76,43 @@ __global__ void __launch_bounds__(D) splitkv_reduce_kernel(const AttnParams p) {
   const float* pm = p.part_m + static_cast<size_t>(orow) * p.max_parts;
   const float* pl = p.part_l + static_cast<size_t>(orow) * p.max_parts;
   const float* po = p.part_o + static_cast<size_t>(orow) * p.max_parts * D;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // M = max_i m_i
   float M = -CUDART_INF_F;
-  for (int i = 0; i < nparts; ++i) M = fmaxf(M, pm[i]);
-  const int d = threadIdx.x;
+  for (int i = tid; i < nparts; i += D) M = fmaxf(M, pm[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) M = fmaxf(M, s_red[w]);
+
   float S = 0.f, o = 0.f;
-  if (M != -CUDART_INF_F) {
-    for (int i = 0; i < nparts; ++i) {
-      const float mi = pm[i];
-      const float w = (mi == -CUDART_INF_F) ? 0.f : pl[i] * exp2f(mi - M);
-      S += w;
-      o += w * po[static_cast<size_t>(i) * D + d];
+  for (int c0 = 0; c0 < nparts; c0 += kChunk) {
+    const int n = min(kChunk, nparts - c0);
+    __syncthreads();                          // s_w / s_red reuse
+    if (tid < n) {
+      const float mi = pm[c0 + tid];
+      s_w[tid] = (mi == -CUDART_INF_F || M == -CUDART_INF_F) ? 0.f
+                                                           : pl[c0 + tid] * exp2f(mi - M);
+    }
+    __syncthreads();
+    const float* pc = po + static_cast<size_t>(c0) * D + tid;
+    int i = 0;
+    for (; i + 4 <= n; i += 4) {
+      const float x0 = pc[(i + 0) * D], x1 = pc[(i + 1) * D];
+      const float x2 = pc[(i + 2) * D], x3 = pc[(i + 3) * D];
+      o += s_w[i] * x0 + s_w[i + 1] * x1 + s_w[i + 2] * x2 + s_w[i + 3] * x3;
+      S += s_w[i] + s_w[i + 1] + s_w[i + 2] + s_w[i + 3];
+    }
+    for (; i < n; ++i) {
+      o += s_w[i] * pc[i * D];
+      S += s_w[i];
     }
   }
-  reinterpret_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(orow) * D + d] =
+  reinterpret_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(orow) * D + tid] =
       __float2bfloat16_rn(S > 0.f ? o / S : 0.f);
 }
 

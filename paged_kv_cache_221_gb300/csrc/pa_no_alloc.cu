@@ -13,7 +13,7 @@
 // is loaded on.
 #include <mutex>
 
-#include "../../include/paged_attn.h"
+#include "paged_attn.h"
 #include "pa_internal.h"
 
 namespace {

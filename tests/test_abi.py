@@ -44,10 +44,13 @@ def test_workspace_size_host_only(lib):
     assert lib.pa_workspace_size(64, 32, 1, 512, 128, 16, 0, 0) == 0
     # 4096 tokens in 512-token partitions: 8 slots per row, (D + 2) floats per slot, 256-B rounded
     rows = 64 * 32
-    want = (rows * 8 * 128 * 4 + 255) // 256 * 256 + 2 * ((rows * 8 * 4 + 255) // 256 * 256)
-    assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 512, 0) == want
-    assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 0, 0) == want   # default 512
-    assert lib.pa_default_partition_size(64, 8, 4096, 16) == 512
+
+    def want(slots):
+        return (rows * slots * 128 * 4 + 255) // 256 * 256 + 2 * ((rows * slots * 4 + 255) // 256 * 256)
+
+    assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 512, 0) == want(8)
+    assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 0, 0) == want(4)   # default 1024
+    assert lib.pa_default_partition_size(64, 8, 4096, 16) == 1024
     assert lib.pa_default_partition_size(64, 8, 100, 16) == 112
     # shared prefix always needs scratch
     assert lib.pa_workspace_size(2, 4, 1, 64, 64, 16, 64, 2) > 0

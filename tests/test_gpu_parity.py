@@ -306,3 +306,45 @@ def test_full_size_sampled(name):
     # reshape_and_cache: every written slot holds its token, bit for bit
     kb = bits(d.k)
     np.testing.assert_array_equal(kb[s // 16, :, s % 16, :], w.new_key)
+
+
+# ----------------------------------------------------------------------------- softmax range
+
+def _f32(bits_u16):
+    return (bits_u16.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def test_peaked_scores_rescale_many_times():
+    """Queries scaled x40: scores span ~100 (log2 units), the running max jumps often."""
+    w = W.SMALL["spec_verify"]()
+    w.q = W.f32_to_bf16_bits(_f32(w.q) * 40.0)
+    ref, _, _ = O.run_workload(w)
+    d = Dev(w)
+    d.reshape()
+    for ps in (64, 0):
+        assert_close(d.attend(partition_size=ps), ref, what=f"peaked ps{ps}")
+
+
+def test_scores_growing_along_the_context():
+    """K rows scaled up with their position: the max rises page after page."""
+    w = W.SMALL["decode_70b"]()
+    k = _f32(w.k_cache).copy()
+    nk = _f32(w.new_key).copy()
+    for b in range(w.num_seqs):
+        L = int(w.context_lens[b])
+        for j in range(L):
+            f = 1.0 + 6.0 * j / L
+            blk, off = w.block_tables[b, j // 16], j % 16
+            if j >= L - w.num_query_tokens:
+                nk[b * w.num_query_tokens + (j - (L - w.num_query_tokens))] *= f
+            else:
+                k[blk, :, off, :] *= f
+    finite = np.isfinite(k)
+    kb = W.f32_to_bf16_bits(np.where(finite, k, 0.0))
+    w.k_cache = np.where(finite, kb, w.k_cache)
+    w.new_key = W.f32_to_bf16_bits(nk)
+    ref, _, _ = O.run_workload(w)
+    d = Dev(w)
+    d.reshape()
+    for ps in (32, 0):
+        assert_close(d.attend(partition_size=ps), ref, what=f"growing ps{ps}")
