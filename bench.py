@@ -273,17 +273,22 @@ def run_gb300(args):
     out = torch.empty_like(q)
     kv_bytes = w.kv_bytes()
 
+    # Per-sequence workloads: one fused call (reshape_and_cache inside the attention
+    # launch).  Shared-prefix workload: reshape_and_cache, then the shared-prefix call.
     def reshape():
-        pa.reshape_and_cache(nk, nv, k, v, slots)
+        if grouped:
+            pa.reshape_and_cache(nk, nv, k, v, slots)
 
     def attend():
         if grouped:
             pa.decode_shared_prefix(q, k, v, tables, lens, sg, gp, w.max_group_size,
                                     w.max_prefix_blocks, w.max_context_len, w.scale, ps, ws, out)
         else:
-            pa.verify(q, k, v, tables, lens, w.max_context_len, w.scale, ps, ws, out)
+            pa.verify(q, k, v, tables, lens, w.max_context_len, w.scale, ps, ws, out,
+                      nk, nv)
 
-    launches_per_step = 1 + 1 + (1 if need > 0 else 0) + (1 if grouped else 0)
+    # our kernels per step: attention (+ split-KV merge) (+ reshape + shared-prefix kernel)
+    launches_per_step = 1 + (1 if need > 0 else 0) + (2 if grouped else 0)
 
     stream = torch.cuda.current_stream(dev)
     # warm-up outside capture (sets kernel attributes), then capture one graph per phase
@@ -292,15 +297,24 @@ def run_gb300(args):
         attend()
     torch.cuda.synchronize(dev)
     assert pa.get_device_error(dev) == 0
-    g_reshape, g_attend = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_reshape = torch.cuda.CUDAGraph() if grouped else None
+    g_attend = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        with torch.cuda.graph(g_reshape, stream=side):
-            reshape()
+        if grouped:
+            with torch.cuda.graph(g_reshape, stream=side):
+                reshape()
         with torch.cuda.graph(g_attend, stream=side):
             attend()
     stream.wait_stream(side)
+
+    class _NoGraph:
+        def replay(self):
+            pass
+
+    if g_reshape is None:
+        g_reshape = _NoGraph()
     for _ in range(max(3, args.warmup)):
         g_reshape.replay()
         g_attend.replay()
@@ -397,8 +411,8 @@ def run_gb300(args):
         e2e = {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
-               "path": "pinned host inputs -> H2D -> pa_reshape_and_cache + attention call "
-                       "(Python binding, no graph) -> D2H of the bf16 output"}
+               "path": "pinned host inputs -> H2D -> the step's library calls (Python binding, "
+                       "no graph) -> D2H of the bf16 output"}
 
     if rank != 0:
         if world > 1:
@@ -425,8 +439,8 @@ def run_gb300(args):
                      "launch_ms_median": round(statistics.median(attn_ms), 5)},
         "clocks": clocks,
         "gpu_launches": launches_per_step * steps,
-        "timing": "CUDA graphs of the two phases replayed per step; events on the launching "
-                  "stream",
+        "timing": "CUDA graph of the step replayed (shared-prefix: reshape graph + attention "
+                  "graph); CUDA events on the launching stream around the attention call",
     }
     if e2e is not None:
         line["e2e"] = e2e

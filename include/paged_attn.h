@@ -119,9 +119,11 @@ int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_le
  *
  * Long contexts are split into partitions of partition_size tokens (0 = the
  * library default) that are processed in parallel and merged with the
- * log-sum-exp rule; this needs `workspace` of at least pa_workspace_size(...)
- * bytes.  With partition_size = 0 and workspace == NULL every sequence is
- * processed whole (no scratch, fewer parallel units).  With an explicit
+ * log-sum-exp rule by a second kernel; this needs `workspace` of at least
+ * pa_workspace_size(...) bytes.  The workspace needs no initialisation (every
+ * partial is written before it is read) and may be reused by later calls on
+ * the same stream.  With partition_size = 0 and workspace == NULL every
+ * sequence is processed whole (no scratch, fewer parallel units).  With an explicit
  * partition_size that needs scratch, a missing or short workspace returns
  * PA_ERR_WORKSPACE.
  *
@@ -153,6 +155,27 @@ pa_status pa_verify(void* out, const void* q, const void* k_cache, const void* v
                     int num_query_tokens, int num_blocks, int num_q_heads, int num_kv_heads,
                     int head_dim, int block_size, float scale, int partition_size,
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode_append — reshape_and_cache fused into the attention call: the K
+ * and V vectors of every sequence's num_query_tokens (T) query tokens,
+ *   new_key, new_value  [num_seqs, T, num_kv_heads, head_dim]  bf16,
+ * are stored at positions context_lens[b] - T + t of their sequence (block
+ * block_tables[b, pos / block_size], slot pos % block_size, bit-exact) by the
+ * attention CTA that reads that page, immediately before it reads it; then the
+ * call computes pa_verify (pa_decode for T = 1).  Same result as
+ * pa_reshape_and_cache with those slots followed by pa_verify, in one launch.
+ * Cited: "LLM inference optimization: KV cache", §3.1 and its diagram (the
+ * new token's K and V are saved into the cache, then attention reads the cache).
+ * k_cache / v_cache are written; other arguments and errors as pa_verify.
+ */
+pa_status pa_decode_append(void* out, const void* q, const void* new_key, const void* new_value,
+                           void* k_cache, void* v_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens,
+                           int max_context_len, int num_seqs, int num_query_tokens,
+                           int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, float scale, int partition_size, void* workspace,
+                           size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * pa_decode_shared_prefix — pa_decode for batches where groups of sequences

@@ -130,14 +130,31 @@ def verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
            block_tables: torch.Tensor, context_lens: torch.Tensor,
            max_context_len: Optional[int] = None, scale: Optional[float] = None,
            partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
-           out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Attention of T draft tokens per sequence ([B, T, Hq, D]) with a causal mask among drafts."""
+           out: Optional[torch.Tensor] = None, new_key: Optional[torch.Tensor] = None,
+           new_value: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Attention of T draft tokens per sequence ([B, T, Hq, D]) with a causal mask among drafts.
+
+    With ``new_key`` / ``new_value`` ([B*T, Hkv, D] or [B, T, Hkv, D]) the query tokens' K/V
+    are first stored at positions L-T .. L-1 of every sequence, inside the same launch
+    (reshape_and_cache fused).
+    """
     dev, B, T, Hq, D, NB, Hkv, BS, mcl, out = _attn_common(q, k_cache, v_cache, block_tables,
                                                           context_lens, max_context_len, out)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     need = workspace_size(B, Hq, T, mcl, D, BS, partition_size, 0) if B else 0
     ws, wsb = _workspace(dev, workspace, need)
     lib = library()
+    if new_key is not None or new_value is not None:
+        for name, t in (("new_key", new_key), ("new_value", new_value)):
+            if t is None or t.numel() != B * T * Hkv * D:
+                raise ValueError(f"{name} must hold [B, T, Hkv, D] values")
+            _need(name, t, torch.bfloat16, t.dim(), dev)
+        st = lib.pa_decode_append(_vp(out), _vp(q), _vp(new_key), _vp(new_value), _vp(k_cache),
+                                  _vp(v_cache), _vp(block_tables), block_tables.shape[1],
+                                  _vp(context_lens), mcl, B, T, NB, Hq, Hkv, D, BS, scale,
+                                  partition_size, _vp(ws), wsb, _stream(dev))
+        _lib.check("pa_decode_append", st)
+        return out
     if T == 1:
         st = lib.pa_decode(_vp(out), _vp(q), _vp(k_cache), _vp(v_cache), _vp(block_tables),
                            block_tables.shape[1], _vp(context_lens), mcl, B, NB, Hq, Hkv, D, BS,
@@ -155,15 +172,20 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
            block_tables: torch.Tensor, context_lens: torch.Tensor,
            max_context_len: Optional[int] = None, scale: Optional[float] = None,
            partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
-           out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Single-token decode attention; q is [B, Hq, D] or [B, 1, Hq, D] (out has q's shape)."""
+           out: Optional[torch.Tensor] = None, new_key: Optional[torch.Tensor] = None,
+           new_value: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Single-token decode attention; q is [B, Hq, D] or [B, 1, Hq, D] (out has q's shape).
+
+    With ``new_key`` / ``new_value`` ([B, Hkv, D]) the new token's K/V is stored at position
+    L-1 of every sequence inside the same launch before attention reads it.
+    """
     squeeze = q.dim() == 3
     q4 = q.unsqueeze(1) if squeeze else q
     if q4.shape[1] != 1:
         raise ValueError("decode takes one query token per sequence (use verify for drafts)")
     o4 = None if out is None else (out.unsqueeze(1) if squeeze else out)
     r = verify(q4, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
-               partition_size, workspace, o4)
+               partition_size, workspace, o4, new_key, new_value)
     return r.squeeze(1) if squeeze else r
 
 

@@ -29,6 +29,8 @@ SIGNATURES = {
                        _vp, _sz, _vp]),
     "pa_verify": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                        _i, _vp, _sz, _vp]),
+    "pa_decode_append": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
+                              _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "pa_decode_shared_prefix": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                      _i, _f, _i, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
     "pa_decode_static_scratch": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,

@@ -61,6 +61,7 @@ int default_partition_tokens(int max_context_len) {
   return max_context_len > 1024 ? 1024 : ceil_div(max_context_len, kBlockSize) * kBlockSize;
 }
 
+// Scratch layout: [O partials][m][l], each region 256-byte aligned.
 Plan make_plan(int num_seqs, int hq, int T, int max_ctx, int head_dim, int partition_size,
                int max_prefix_blocks) {
   Plan pl;
@@ -82,6 +83,8 @@ Plan make_plan(int num_seqs, int hq, int T, int max_ctx, int head_dim, int parti
 struct AttnArgs {
   void* out;
   const void* q;
+  const void* new_k;       // query tokens' K/V to append (nullptr: already in the pool)
+  const void* new_v;
   const void* k_cache;
   const void* v_cache;
   const int32_t* block_tables;
@@ -162,6 +165,13 @@ pa_status run_attention(const AttnArgs& a) {
     p.part_m = reinterpret_cast<float*>(ws + plan.off_m);
     p.part_l = reinterpret_cast<float*>(ws + plan.off_l);
   }
+  if (a.new_k != nullptr) {
+    if (!a.new_v || !aligned16(a.new_k) || !aligned16(a.new_v)) return PA_ERR_INVALID_ARG;
+    p.new_k = a.new_k;
+    p.new_v = a.new_v;
+    p.k_pool = const_cast<void*>(a.k_cache);
+    p.v_pool = const_cast<void*>(a.v_cache);
+  }
   p.seq_group = grouped ? a.seq_group : nullptr;
   p.group_prefix_blocks = grouped ? a.group_prefix_blocks : nullptr;
   p.mbs = a.max_blocks_per_seq;
@@ -194,7 +204,11 @@ pa_status run_attention(const AttnArgs& a) {
   }
   {
     const int rows = G * a.T;
-    dim3 grid(ceil_div(max_blocks, plan.ppb), a.hkv, a.num_seqs);
+    // 1-D, partition-major: unit u = (partition * num_seqs + seq) * hkv + head
+    const long long units = static_cast<long long>(ceil_div(max_blocks, plan.ppb)) * a.hkv *
+                            a.num_seqs;
+    if (units >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+    dim3 grid(static_cast<unsigned>(units), 1, 1);
     e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream)
                          : launch_attn_d128(tk, tv, p, rows, grid, a.stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
@@ -271,9 +285,9 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
                     int block_size, float scale, int partition_size, void* workspace,
                     size_t workspace_bytes, pa_stream_t stream) {
-  AttnArgs a{out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-             max_context_len, num_seqs, 1, num_blocks, num_q_heads, num_kv_heads, head_dim,
-             block_size, scale, partition_size, nullptr, nullptr, 0, 0, 0, workspace,
+  AttnArgs a{out, q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+             context_lens, max_context_len, num_seqs, 1, num_blocks, num_q_heads, num_kv_heads,
+             head_dim, block_size, scale, partition_size, nullptr, nullptr, 0, 0, 0, workspace,
              workspace_bytes, reinterpret_cast<cudaStream_t>(stream)};
   return run_attention(a);
 }
@@ -284,10 +298,27 @@ pa_status pa_verify(void* out, const void* q, const void* k_cache, const void* v
                     int num_query_tokens, int num_blocks, int num_q_heads, int num_kv_heads,
                     int head_dim, int block_size, float scale, int partition_size,
                     void* workspace, size_t workspace_bytes, pa_stream_t stream) {
-  AttnArgs a{out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-             max_context_len, num_seqs, num_query_tokens, num_blocks, num_q_heads, num_kv_heads,
-             head_dim, block_size, scale, partition_size, nullptr, nullptr, 0, 0, 0, workspace,
-             workspace_bytes, reinterpret_cast<cudaStream_t>(stream)};
+  AttnArgs a{out, q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+             context_lens, max_context_len, num_seqs, num_query_tokens, num_blocks,
+             num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_size, nullptr,
+             nullptr, 0, 0, 0, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream)};
+  return run_attention(a);
+}
+
+pa_status pa_decode_append(void* out, const void* q, const void* new_key, const void* new_value,
+                           void* k_cache, void* v_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens,
+                           int max_context_len, int num_seqs, int num_query_tokens,
+                           int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, float scale, int partition_size, void* workspace,
+                           size_t workspace_bytes, pa_stream_t stream) {
+  if (num_seqs > 0 && (!new_key || !new_value)) return PA_ERR_INVALID_ARG;
+  AttnArgs a{out, q, new_key, new_value, k_cache, v_cache, block_tables, max_blocks_per_seq,
+             context_lens, max_context_len, num_seqs, num_query_tokens, num_blocks,
+             num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_size, nullptr,
+             nullptr, 0, 0, 0, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream)};
   return run_attention(a);
 }
 
@@ -301,10 +332,10 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
                                   int num_groups, int max_group_size, int max_prefix_blocks,
                                   void* workspace, size_t workspace_bytes, pa_stream_t stream) {
   if (num_groups < 0) return PA_ERR_INVALID_ARG;
-  AttnArgs a{out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-             max_context_len, num_seqs, 1, num_blocks, num_q_heads, num_kv_heads, head_dim,
-             block_size, scale, partition_size, seq_group, group_prefix_blocks, num_groups,
-             max_group_size, max_prefix_blocks, workspace, workspace_bytes,
+  AttnArgs a{out, q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+             context_lens, max_context_len, num_seqs, 1, num_blocks, num_q_heads, num_kv_heads,
+             head_dim, block_size, scale, partition_size, seq_group, group_prefix_blocks,
+             num_groups, max_group_size, max_prefix_blocks, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream)};
   return run_attention(a);
 }

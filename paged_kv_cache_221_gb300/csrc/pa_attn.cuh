@@ -100,9 +100,17 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   __shared__ int s_nmem;
   __shared__ int s_bad;
 
+  // The split-KV merge kernel that follows may be scheduled as soon as every
+  // CTA of this grid has started; it waits for this grid's completion itself.
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = blockIdx.y;                 // kv head
+  // Per-sequence mode: a 1-D grid in partition-major order (every sequence's
+  // first partition, then every second one, ...) so that the short, ragged last
+  // partitions are dispatched last.  Shared-prefix mode: (partition, head, group chunk).
+  const int unit_p = GROUP ? static_cast<int>(blockIdx.x)
+                           : static_cast<int>(blockIdx.x / (p.Hkv * p.num_seqs));
+  const int g = GROUP ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x % p.Hkv);
   const int G = p.G, T = p.T;
 
   // ------------------------------------------------------------------ unit
@@ -110,22 +118,22 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   bool direct;
   int b_single = 0;                          // per-sequence mode: the sequence
   if constexpr (!GROUP) {
-    const int b = blockIdx.z;
+    const int b = static_cast<int>((blockIdx.x / p.Hkv) % p.num_seqs);
     const int L = p.context_lens[b];
     const int pre = (p.seq_group != nullptr && p.seq_group[b] >= 0)
                         ? p.group_prefix_blocks[p.seq_group[b]] : 0;
     if (L < T || L > p.max_ctx || pre < 0 || pre > p.max_prefix_blocks ||
         pre * kBlockSize > L) {
-      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_pa_err, kErrBounds);
+      if (threadIdx.x == 0 && unit_p == 0) atomicOr(&g_pa_err, kErrBounds);
       return;
     }
     const int nblk = (L + kBlockSize - 1) / kBlockSize;
-    pg0 = pre + blockIdx.x * p.ppb;
+    pg0 = pre + unit_p * p.ppb;
     if (pg0 >= nblk) return;                 // partition past this sequence's end
     pg1 = min(pg0 + p.ppb, nblk);
     const int npre = (pre + p.ppb - 1) / p.ppb;
     const int nparts = npre + (nblk - pre + p.ppb - 1) / p.ppb;
-    slot = npre + blockIdx.x;
+    slot = npre + unit_p;
     direct = (pre == 0 && nparts == 1);
     nrows = G * T;
     vlen = L;
@@ -158,7 +166,9 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
           if (r >= 0 && r < mc) {
             members[r] = b;
             const int L = p.context_lens[b];
-            if (L < T || L > p.max_ctx || L < pre * kBlockSize) bad = 1;
+            if (L < T || L > p.max_ctx || L < pre * kBlockSize ||
+                (p.new_k != nullptr && L - T < pre * kBlockSize))
+              bad = 1;
           }
         }
         cnt += __popc(bal);
@@ -206,6 +216,29 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       const int cnt = min(32, npages - base);
       for (int j = 0; j < cnt; ++j) {
         const int phys = __shfl_sync(0xffffffffu, phys_l, j);
+        if constexpr (!GROUP) {
+          // Query tokens' K/V that land in this page are stored into the pool
+          // first (reshape_and_cache fused), then the page is read by TMA.
+          const int pos0 = (pg0 + base + j) * kBlockSize;
+          const int lo = max(vlen - T, pos0), hi = min(vlen - 1, pos0 + kBlockSize - 1);
+          if (p.new_k != nullptr && lo <= hi &&
+              static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks)) {
+            constexpr int CH = D / 8;           // 16-byte chunks per row
+            for (int pos = lo; pos <= hi; ++pos) {
+              const size_t src = (static_cast<size_t>(b_single) * T + (pos - (vlen - T))) * p.Hkv + g;
+              const size_t dst = (static_cast<size_t>(phys) * p.Hkv + g) * kBlockSize +
+                                 (pos & (kBlockSize - 1));
+              for (int c = lane; c < 2 * CH; c += 32) {
+                const bool isv = c >= CH;
+                const int cc = isv ? c - CH : c;
+                const uint4 v = reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + cc];
+                reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + cc] = v;
+              }
+            }
+            fence_proxy_async_global();
+            __syncwarp();
+          }
+        }
         if (lane == 0) {
           const int it = base + j;
           const int s = it % kStages;

@@ -22,6 +22,10 @@ struct AttnParams {
   void* out;                      // bf16 [B, T, Hq, D]
   const int32_t* block_tables;    // [B, mbs]
   const int32_t* context_lens;    // [B]
+  const void* new_k;              // bf16 [B, T, Hkv, D] or nullptr: K of the query tokens,
+  const void* new_v;              //   written at positions L-T .. L-1 before they are read
+  void* k_pool;                   // the pools again, for those writes
+  void* v_pool;
   float* part_o;                  // [B*T*Hq, max_parts, D]   (split-KV partials)
   float* part_m;                  // [B*T*Hq, max_parts]      running max, log2 domain
   float* part_l;                  // [B*T*Hq, max_parts]      softmax denominator

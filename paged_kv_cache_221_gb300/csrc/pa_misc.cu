@@ -62,6 +62,9 @@ __global__ void __launch_bounds__(D) splitkv_reduce_kernel(const AttnParams p) {
   constexpr int kWarps = D / 32;
   __shared__ float s_w[kChunk];
   __shared__ float s_red[kWarps];
+  // Launched as a programmatic dependent of the attention kernel: wait for its
+  // completion (and the visibility of its partials) before reading anything.
+  grid_dependency_wait();
   const int orow = blockIdx.x;
   const int b = orow / (p.T * p.Hq);
   const int L = p.context_lens[b];
@@ -119,11 +122,21 @@ __global__ void __launch_bounds__(D) splitkv_reduce_kernel(const AttnParams p) {
 cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s) {
   const long long rows = static_cast<long long>(p.num_seqs) * p.T * p.Hq;
   if (rows == 0) return cudaSuccess;
-  if (head_dim == 64)
-    splitkv_reduce_kernel<64><<<static_cast<unsigned>(rows), 64, 0, s>>>(p);
-  else
-    splitkv_reduce_kernel<128><<<static_cast<unsigned>(rows), 128, 0, s>>>(p);
-  return cudaGetLastError();
+  // Programmatic stream serialisation: the launch may overlap the tail of the
+  // attention kernel; the kernel's first instruction waits for it to finish.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
+  cfg.blockDim = dim3(head_dim == 64 ? 64 : 128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const AttnParams args = p;
+  return head_dim == 64 ? cudaLaunchKernelEx(&cfg, splitkv_reduce_kernel<64>, args)
+                        : cudaLaunchKernelEx(&cfg, splitkv_reduce_kernel<128>, args);
 }
 
 // ---------------------------------------------------------------- self test

@@ -40,6 +40,13 @@ class Dev:
     def reshape(self):
         pa.reshape_and_cache(self.new_key, self.new_value, self.k, self.v, self.slots)
 
+    def attend_append(self, partition_size=None, workspace=None, out=None):
+        """reshape_and_cache fused into the attention launch (pa_decode_append)."""
+        w = self.w
+        ps = w.partition_size if partition_size is None else partition_size
+        return pa.verify(self.q, self.k, self.v, self.tables, self.lens, w.max_context_len,
+                         w.scale, ps, workspace, out, self.new_key, self.new_value)
+
     def attend(self, partition_size=None, shared=True, workspace=None, out=None):
         w = self.w
         ps = w.partition_size if partition_size is None else partition_size

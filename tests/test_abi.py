@@ -45,8 +45,11 @@ def test_workspace_size_host_only(lib):
     # 4096 tokens in 512-token partitions: 8 slots per row, (D + 2) floats per slot, 256-B rounded
     rows = 64 * 32
 
-    def want(slots):
-        return (rows * slots * 128 * 4 + 255) // 256 * 256 + 2 * ((rows * slots * 4 + 255) // 256 * 256)
+    def r256(x):
+        return (x + 255) // 256 * 256
+
+    def want(slots):        # [O partials][m][l]
+        return r256(rows * slots * 128 * 4) + 2 * r256(rows * slots * 4)
 
     assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 512, 0) == want(8)
     assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 0, 0) == want(4)   # default 1024

@@ -287,11 +287,17 @@ def sample_seqs(w, n=6, seed=0):
 @pytest.mark.parametrize("name", ["tiny", "decode_8b", "decode_70b", "spec_verify",
                                   "shared_prefix"])
 def test_full_size_sampled(name):
-    """Full-size workload in the benchmark's launch configuration; sampled rows vs the oracle."""
+    """Full-size workload in the benchmark's launch configuration; sampled rows vs the oracle.
+
+    The benchmark runs the fused append call for the per-sequence workloads and
+    reshape_and_cache + the shared-prefix call for the shared-prefix workload."""
     w = W.FULL[name]()
     d = Dev(w)
-    d.reshape()
-    out = d.attend()
+    if w.seq_group is None:
+        out = d.attend_append()
+    else:
+        d.reshape()
+        out = d.attend()
     torch.cuda.synchronize()
     assert bool(torch.isfinite(out.float()).all())
     seqs = sample_seqs(w, n=4 if name == "shared_prefix" else 6)
@@ -348,3 +354,35 @@ def test_scores_growing_along_the_context():
     d.reshape()
     for ps in (32, 0):
         assert_close(d.attend(partition_size=ps), ref, what=f"growing ps{ps}")
+
+
+# ----------------------------------------------------------------------------- fused append
+
+@pytest.mark.parametrize("name", ["tiny", "decode_8b", "decode_70b", "spec_verify"])
+@pytest.mark.parametrize("psize", [32, 0])
+def test_append_equals_reshape_then_attend(name, psize):
+    """pa_decode_append writes the same pool bits and the same output bits as
+    pa_reshape_and_cache followed by the attention call, and matches the oracle."""
+    w = W.SMALL[name]()
+    ref, kref, vref = O.run_workload(w)
+    a = Dev(w)
+    out_a = a.attend_append(partition_size=psize).clone()
+    np.testing.assert_array_equal(bits(a.k), kref)
+    np.testing.assert_array_equal(bits(a.v), vref)
+    b = Dev(w)
+    b.reshape()
+    out_b = b.attend(partition_size=psize)
+    assert torch.equal(bits_t(out_a), bits_t(out_b))
+    assert_close(out_a, ref, what=f"append {name}")
+
+
+def test_append_edge_lengths():
+    lens = [max(L, 3) for L in EDGE_LENS]
+    w = W.build("edge_append", lens, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                num_query_tokens=3, seed=77)
+    ref, kref, _ = O.run_workload(w)
+    d = Dev(w)
+    for ps in (16, 0):
+        out = d.attend_append(partition_size=ps)
+        assert_close(out, ref, what=f"append edge ps{ps}")
+    np.testing.assert_array_equal(bits(d.k), kref)
