@@ -129,6 +129,8 @@ int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_le
  *
  * max_context_len must bound every context_lens[b] and be at most
  * max_blocks_per_seq*block_size; it sizes the launch without a device read.
+ * At most 4096 partitions per sequence (PA_ERR_UNSUPPORTED beyond: choose a
+ * larger partition_size).
  * Requirements: head_dim 64 or 128, block_size 16, num_q_heads a multiple of
  * num_kv_heads with at most 64 query heads per kv head, q/out/k_cache/v_cache
  * 16-byte aligned, num_blocks*num_kv_heads*block_size < 2^31.

@@ -55,10 +55,13 @@ struct Plan {
   size_t off_m = 0, off_l = 0;
 };
 
-// 1024-token partitions (64 pages per CTA) measured best on GB300 for contexts of
-// 512 .. 32768 tokens; shorter contexts stay whole.
+// Partition sizes measured best on GB300: contexts up to 4096 tokens in
+// 1024-token partitions (64 pages per CTA), longer ones in 2048-token
+// partitions (fewer partials to merge); contexts up to 1024 tokens stay whole.
 int default_partition_tokens(int max_context_len) {
-  return max_context_len > 1024 ? 1024 : ceil_div(max_context_len, kBlockSize) * kBlockSize;
+  if (max_context_len > 4096) return 2048;
+  if (max_context_len > 1024) return 1024;
+  return ceil_div(max_context_len, kBlockSize) * kBlockSize;
 }
 
 // Scratch layout: [O partials][m][l], each region 256-byte aligned.
@@ -144,6 +147,7 @@ pa_status run_attention(const AttnArgs& a) {
   }
   const Plan plan = make_plan(a.num_seqs, a.hq, a.T, a.max_context_len, a.head_dim, psize,
                               max_prefix);
+  if (plan.max_parts > kMaxPartitions) return PA_ERR_UNSUPPORTED;   // use larger partitions
   if (plan.ws_bytes > 0) {
     if (!a.workspace || a.workspace_bytes < plan.ws_bytes) return PA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(a.workspace) & 255u) return PA_ERR_INVALID_ARG;

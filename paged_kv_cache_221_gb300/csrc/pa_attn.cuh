@@ -25,6 +25,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "pa_ptx.cuh"
 
 namespace pa {
@@ -100,9 +102,6 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   __shared__ int s_nmem;
   __shared__ int s_bad;
 
-  // The split-KV merge kernel that follows may be scheduled as soon as every
-  // CTA of this grid has started; it waits for this grid's completion itself.
-  grid_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Per-sequence mode: a 1-D grid in partition-major order (every sequence's
@@ -289,7 +288,10 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       *reinterpret_cast<uint4*>(qs + n * Gm::kQStride + ch * 8) = v;
     }
     for (int n = threadIdx.x; n < Sm::kRows; n += NCT) {
-      int lm = -1;                            // padding rows see nothing
+      // Padding rows (query 0) see every position: their columns of the tiles
+      // are never written out, and treating them as unmasked lets interior
+      // pages skip masking altogether.
+      int lm = 0x7fffffff;
       if (n < nrows) {
         const int m = n / (G * T), t = (n / G) % T;
         lm = p.context_lens[GROUP ? members[m] : b_single] - T + t;
@@ -342,6 +344,20 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   const int mi = lane >> 3, rr = lane & 7;
   const int ktok = rr + ((mi & 1) << 3), kch = mi >> 1;     // K: A operand (tokens x dims)
   const int vtok = rr + ((mi >> 1) << 3), vch = mi & 1;     // V: A operand (dims x tokens)
+  // Swizzled byte offsets of this lane's ldmatrix rows for 16-byte chunks
+  // 2k + sel (k = 0..3) of the first 64 head dims; the second 64 add one box.
+  uint32_t koff[4], voff[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    koff[k] = page_off(ktok, 2 * k + kch);
+    voff[k] = page_off(vtok, 2 * k + vch);
+  }
+  // Smallest visibility limit of this warp's rows: pages wholly below it (and
+  // below the context end) need no masking.
+  int minlim = 0x7fffffff;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) minlim = min(minlim, min(lim0[j], lim1[j]));
+  minlim = __reduce_min_sync(0xffffffffu, minlim);
 
   for (int it = pl; it < npages; it += PL) {
     const int s = it % kStages;
@@ -361,8 +377,10 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 #pragma unroll
       for (int k2 = 0; k2 < Gm::kKSteps; k2 += 2) {
         uint32_t a[2][4];
-        ldsm_x4(a[0][0], a[0][1], a[0][2], a[0][3], kb + page_off(ktok, 2 * k2 + kch));
-        ldsm_x4(a[1][0], a[1][1], a[1][2], a[1][3], kb + page_off(ktok, 2 * k2 + 2 + kch));
+        ldsm_x4(a[0][0], a[0][1], a[0][2], a[0][3],
+                kb + (k2 >> 2) * Gm::kHalfBytes + koff[k2 & 3]);
+        ldsm_x4(a[1][0], a[1][1], a[1][2], a[1][3],
+                kb + ((k2 + 1) >> 2) * Gm::kHalfBytes + koff[(k2 + 1) & 3]);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           uint32_t b00, b01, b10, b11;
@@ -383,6 +401,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       // V rows at or past the context end may hold anything (even NaN): their
       // weight is 0, but 0 * NaN is NaN, so zero them in the operand.
       const int nvalid = vlen - tok0;
+      const bool interior = (tok0 + kBlockSize - 1 <= minlim) && (nvalid >= kBlockSize);
       uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
       if (nvalid < kBlockSize) {
         mlo = (2 * q4 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < nvalid ? 0xffff0000u : 0u);
@@ -395,10 +414,14 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         // lane holds S^T[j0][n], S^T[j0][n+1], S^T[j0+8][n], S^T[j0+8][n+1], n = rbase+8j+2q4
-        const float t0 = (j0 <= lim0[j]) ? (sa[j][0] + sb[j][0]) * sl2 : -CUDART_INF_F;
-        const float t1 = (j0 <= lim1[j]) ? (sa[j][1] + sb[j][1]) * sl2 : -CUDART_INF_F;
-        const float t2 = (j1 <= lim0[j]) ? (sa[j][2] + sb[j][2]) * sl2 : -CUDART_INF_F;
-        const float t3 = (j1 <= lim1[j]) ? (sa[j][3] + sb[j][3]) * sl2 : -CUDART_INF_F;
+        float t0 = (sa[j][0] + sb[j][0]) * sl2, t1 = (sa[j][1] + sb[j][1]) * sl2;
+        float t2 = (sa[j][2] + sb[j][2]) * sl2, t3 = (sa[j][3] + sb[j][3]) * sl2;
+        if (!interior) {
+          t0 = (j0 <= lim0[j]) ? t0 : -CUDART_INF_F;
+          t1 = (j0 <= lim1[j]) ? t1 : -CUDART_INF_F;
+          t2 = (j1 <= lim0[j]) ? t2 : -CUDART_INF_F;
+          t3 = (j1 <= lim1[j]) ? t3 : -CUDART_INF_F;
+        }
 
         // online softmax (log2 domain), statistics per row.  The reference max m
         // only moves when a score exceeds it by more than 8 (so every weight
@@ -411,8 +434,8 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
         }
         const bool up0 = mx0 > m0[j] + 8.f, up1 = mx1 > m1[j] + 8.f;
         if (__any_sync(0xffffffffu, up0 || up1)) {
-          const float al0 = up0 ? exp2f(m0[j] - mx0) : 1.f;
-          const float al1 = up1 ? exp2f(m1[j] - mx1) : 1.f;
+          const float al0 = up0 ? hw_exp2(m0[j] - mx0) : 1.f;
+          const float al1 = up1 ? hw_exp2(m1[j] - mx1) : 1.f;
           if (up0) m0[j] = mx0;
           if (up1) m1[j] = mx1;
           l0[j] *= al0;
@@ -427,8 +450,8 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
         }
         const float mu0 = (m0[j] == -CUDART_INF_F) ? 0.f : m0[j];
         const float mu1 = (m1[j] == -CUDART_INF_F) ? 0.f : m1[j];
-        const float p0 = exp2f(t0 - mu0), p1 = exp2f(t1 - mu1);
-        const float p2 = exp2f(t2 - mu0), p3 = exp2f(t3 - mu1);
+        const float p0 = hw_exp2(t0 - mu0), p1 = hw_exp2(t1 - mu1);
+        const float p2 = hw_exp2(t2 - mu0), p3 = hw_exp2(t3 - mu1);
         l0[j] += p0 + p2;
         l1[j] += p1 + p3;
 
@@ -446,20 +469,28 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       }
 
       // O^T[D x 8] += V_page^T . P^T per n-tile
+      auto pv = [&](auto tail) {
 #pragma unroll
-      for (int mt = 0; mt < Gm::kKSteps; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_trans(a0, a1, a2, a3, vb + page_off(vtok, 2 * mt + vch));
-        a0 &= mlo;
-        a1 &= mlo;
-        a2 &= mhi;
-        a3 &= mhi;
+        for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(a0, a1, a2, a3, vb + (mt >> 2) * Gm::kHalfBytes + voff[mt & 3]);
+          if constexpr (decltype(tail)::value) {
+            a0 &= mlo;
+            a1 &= mlo;
+            a2 &= mhi;
+            a3 &= mhi;
+          }
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bh0[j], bh1[j]);
-          mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bl0[j], bl1[j]);
+          for (int j = 0; j < NT; ++j) {
+            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bh0[j], bh1[j]);
+            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bl0[j], bl1[j]);
+          }
         }
-      }
+      };
+      if (nvalid < kBlockSize)
+        pv(std::true_type{});
+      else
+        pv(std::false_type{});
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);

@@ -14,6 +14,7 @@ enum : unsigned { kErrBounds = 1u, kErrTimeout = 2u };
 constexpr int kBlockSize = 16;        // tokens per physical block (the only size built)
 constexpr int kStages = 8;            // pages in flight per CTA (multiple of every PL)
 constexpr int kMaxRows = 64;          // query rows per CTA (8 n-tiles of 8)
+constexpr int kMaxPartitions = 4096;  // split-KV partitions per sequence (merge smem bound)
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
 
 // Everything an attention launch needs besides the two tensor maps.

@@ -49,24 +49,30 @@ cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, vo
 }
 
 // ---------------------------------------------------------------- split-KV merge
-// One CTA per query row (b, t, h), one thread per head dim.  Partition i of the
-// row holds O_i (normalised), m_i (running max, log2 domain) and l_i (sum of
-// 2^(s - m_i)); the merged row is sum_i w_i O_i / sum_i w_i, w_i = l_i 2^(m_i - M),
-// M = max_i m_i.  Rows whose sequence fit in one partition were written by the
-// attention kernel directly and are skipped here (same predicate).  The
-// statistics of up to kChunk partitions are loaded in parallel (one per
-// thread) and the partial rows are summed with independent loads in flight.
+// One CTA per (sequence b, kv head g, chunk of RB query rows); the rows of
+// (b, g) are its G*T query rows (the q heads that read kv head g, times the
+// query tokens).  Partition i of a row holds O_i (normalised), m_i (reference
+// max, log2 domain) and l_i (sum of 2^(s - m_i)); the merged row is
+// sum_i w_i O_i / sum_i w_i with w_i = l_i 2^(m_i - M), M = max_i m_i.
+// Phase 1 loads every (row, partition) statistic of the CTA at once and turns
+// it into a weight; phase 2 gives each thread 4 head dims of one row and sums
+// the partial rows with independent 16-byte loads.  Sequences that fit in one
+// partition were written by the attention kernel directly and are skipped
+// (same predicate).
+constexpr int kMergeThreads = 128;
+constexpr int kMergeMaxWeights = kMaxPartitions;   // rows x partitions per pass
+
 template <int D>
-__global__ void __launch_bounds__(D) splitkv_reduce_kernel(const AttnParams p) {
-  constexpr int kChunk = D;
-  constexpr int kWarps = D / 32;
-  __shared__ float s_w[kChunk];
-  __shared__ float s_red[kWarps];
-  // Launched as a programmatic dependent of the attention kernel: wait for its
-  // completion (and the visibility of its partials) before reading anything.
-  grid_dependency_wait();
-  const int orow = blockIdx.x;
-  const int b = orow / (p.T * p.Hq);
+__global__ void __launch_bounds__(kMergeThreads) splitkv_reduce_kernel(const AttnParams p) {
+  constexpr int C4 = D / 4;                   // float4 chunks per row
+  constexpr int RB = kMergeThreads / C4;      // rows per CTA: 4 (D 128) or 8 (D 64)
+  __shared__ float s_w[kMergeMaxWeights];
+  __shared__ float s_inv[RB];
+  const int rows = p.G * p.T;
+  const int chunks = (rows + RB - 1) / RB;
+  const int bg = blockIdx.x / chunks;
+  const int r0 = (blockIdx.x % chunks) * RB;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int L = p.context_lens[b];
   if (L < p.T || L > p.max_ctx) return;
   const int pre = (p.seq_group != nullptr && p.seq_group[b] >= 0)
@@ -76,67 +82,73 @@ __global__ void __launch_bounds__(D) splitkv_reduce_kernel(const AttnParams p) {
   const int npre = (pre + p.ppb - 1) / p.ppb;
   const int nparts = npre + (nblk - pre + p.ppb - 1) / p.ppb;
   if (pre == 0 && nparts == 1) return;
-  const float* pm = p.part_m + static_cast<size_t>(orow) * p.max_parts;
-  const float* pl = p.part_l + static_cast<size_t>(orow) * p.max_parts;
-  const float* po = p.part_o + static_cast<size_t>(orow) * p.max_parts * D;
+  const int nr = min(RB, rows - r0);
+  // row r = t * G + hl  ->  orow = (b*T + t)*Hq + g*G + hl
+  auto orow_of = [&](int r) {
+    return (static_cast<size_t>(b) * p.T + r / p.G) * p.Hq + g * p.G + r % p.G;
+  };
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  // M = max_i m_i
-  float M = -CUDART_INF_F;
-  for (int i = tid; i < nparts; i += D) M = fmaxf(M, pm[i]);
+  constexpr int kWarps = kMergeThreads / 32;
+  const int per_pass = max(1, min(nr, kMergeMaxWeights / nparts));
+  for (int q0 = 0; q0 < nr; q0 += per_pass) {
+    const int nq = min(per_pass, nr - q0);
+    __syncthreads();
+    // phase 1: m_i for every (row, partition) -> row max -> weights
+    for (int k = tid; k < nq * nparts; k += kMergeThreads)
+      s_w[k] = p.part_m[orow_of(r0 + q0 + k / nparts) * p.max_parts + k % nparts];
+    __syncthreads();
+    for (int r = warp; r < nq; r += kWarps) {
+      float M = -CUDART_INF_F;
+      for (int i = lane; i < nparts; i += 32) M = fmaxf(M, s_w[r * nparts + i]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) s_red[warp] = M;
-  __syncthreads();
-  M = s_red[0];
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float S = 0.f;
+      for (int i = lane; i < nparts; i += 32) {
+        const float mi = s_w[r * nparts + i];
+        const float w = (mi == -CUDART_INF_F || M == -CUDART_INF_F)
+                            ? 0.f
+                            : p.part_l[orow_of(r0 + q0 + r) * p.max_parts + i] * exp2f(mi - M);
+        s_w[r * nparts + i] = w;
+        S += w;
+      }
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) M = fmaxf(M, s_red[w]);
-
-  float S = 0.f, o = 0.f;
-  for (int c0 = 0; c0 < nparts; c0 += kChunk) {
-    const int n = min(kChunk, nparts - c0);
-    __syncthreads();                          // s_w / s_red reuse
-    if (tid < n) {
-      const float mi = pm[c0 + tid];
-      s_w[tid] = (mi == -CUDART_INF_F || M == -CUDART_INF_F) ? 0.f
-                                                           : pl[c0 + tid] * exp2f(mi - M);
+      for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+      if (lane == 0) s_inv[r] = S > 0.f ? 1.f / S : 0.f;
     }
     __syncthreads();
-    const float* pc = po + static_cast<size_t>(c0) * D + tid;
-    int i = 0;
-    for (; i + 4 <= n; i += 4) {
-      const float x0 = pc[(i + 0) * D], x1 = pc[(i + 1) * D];
-      const float x2 = pc[(i + 2) * D], x3 = pc[(i + 3) * D];
-      o += s_w[i] * x0 + s_w[i + 1] * x1 + s_w[i + 2] * x2 + s_w[i + 3] * x3;
-      S += s_w[i] + s_w[i + 1] + s_w[i + 2] + s_w[i + 3];
-    }
-    for (; i < n; ++i) {
-      o += s_w[i] * pc[i * D];
-      S += s_w[i];
+    // phase 2: O = sum_i w_i O_i / S, 4 head dims per thread
+    const int r = tid / C4, c = tid % C4;
+    if (r < nq) {
+      const size_t orow = orow_of(r0 + q0 + r);
+      const float4* po = reinterpret_cast<const float4*>(p.part_o + orow * p.max_parts * D) + c;
+      const float* w = s_w + r * nparts;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int i = 0; i < nparts; ++i) {
+        const float4 x = po[static_cast<size_t>(i) * C4];
+        acc.x += w[i] * x.x;
+        acc.y += w[i] * x.y;
+        acc.z += w[i] * x.z;
+        acc.w += w[i] * x.w;
+      }
+      const float inv = s_inv[r];
+      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(p.out) + (orow * D + 4 * c) / 2;
+      dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     }
   }
-  reinterpret_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(orow) * D + tid] =
-      __float2bfloat16_rn(S > 0.f ? o / S : 0.f);
 }
 
 cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s) {
-  const long long rows = static_cast<long long>(p.num_seqs) * p.T * p.Hq;
-  if (rows == 0) return cudaSuccess;
-  // Programmatic stream serialisation: the launch may overlap the tail of the
-  // attention kernel; the kernel's first instruction waits for it to finish.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
-  cfg.blockDim = dim3(head_dim == 64 ? 64 : 128, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const AttnParams args = p;
-  return head_dim == 64 ? cudaLaunchKernelEx(&cfg, splitkv_reduce_kernel<64>, args)
-                        : cudaLaunchKernelEx(&cfg, splitkv_reduce_kernel<128>, args);
+  const int rb = kMergeThreads / (head_dim / 4);
+  const long long chunks = (static_cast<long long>(p.G) * p.T + rb - 1) / rb;
+  const long long ctas = static_cast<long long>(p.num_seqs) * p.Hkv * chunks;
+  if (ctas == 0) return cudaSuccess;
+  if (head_dim == 64)
+    splitkv_reduce_kernel<64><<<static_cast<unsigned>(ctas), kMergeThreads, 0, s>>>(p);
+  else
+    splitkv_reduce_kernel<128><<<static_cast<unsigned>(ctas), kMergeThreads, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- self test

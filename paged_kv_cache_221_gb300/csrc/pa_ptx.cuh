@@ -96,17 +96,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- dependent launch
-// Let the next kernel of the stream (launched with programmatic stream
-// serialisation) be scheduled once every CTA of this grid has started.
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Wait until the preceding kernel of the stream has completed and its memory
-// writes are visible (a no-op when the launch had no programmatic dependency).
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+// ---------------------------------------------------------------- exp2
+// 2^x by the hardware approximation (PTX ex2.approx, relative error below
+// 2^-22, subnormal results flushed); 2^-inf = +0.
+__device__ __forceinline__ float hw_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ---------------------------------------------------------------- named barrier

@@ -55,6 +55,7 @@ def test_workspace_size_host_only(lib):
     assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 0, 0) == want(4)   # default 1024
     assert lib.pa_default_partition_size(64, 8, 4096, 16) == 1024
     assert lib.pa_default_partition_size(64, 8, 100, 16) == 112
+    assert lib.pa_default_partition_size(64, 8, 16384, 16) == 2048
     # shared prefix always needs scratch
     assert lib.pa_workspace_size(2, 4, 1, 64, 64, 16, 64, 2) > 0
 
