@@ -64,6 +64,29 @@ def dist_env():
 
 # ----------------------------------------------------------------------------- helpers
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The maximum of ``value`` over all ranks (the slowest replica sets the time)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(bytes_per_rank_step: int, world: int, steps: int, ms_max: float) -> float:
+    """KV bytes read by every rank over ``steps`` steps, divided by the slowest rank's time."""
+    return bytes_per_rank_step * world * steps / (ms_max * 1e-3) / 1e9
+
+
+def replica_workload(name: str, rank: int):
+    """Rank ``rank``'s replica: the named workload drawn with its own seed (same shapes)."""
+    import workloads as W
+    make = W.FULL[name]
+    default_seed = make.__defaults__[0] if make.__defaults__ else 0
+    return make(default_seed + 1000 * rank)
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -247,11 +270,8 @@ def run_gb300(args):
     if world > 1:
         dist.barrier()
     import paged_kv_cache_221_gb300 as pa
-    import workloads as W
 
-    make = W.FULL[args.workload]
-    default_seed = make.__defaults__[0] if make.__defaults__ else 0
-    w = make(default_seed + 1000 * rank)
+    w = replica_workload(args.workload, rank)
     ps = w.partition_size if args.partition_size < 0 else args.partition_size
 
     def td(a):
@@ -362,16 +382,12 @@ def run_gb300(args):
     clocks = sampler.stop()
     assert pa.get_device_error(dev) == 0, "device error during the timed region"
 
-    ms_total = start.elapsed_time(stop)
     attn_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(steps)]
     attn_avg = sum(attn_ms) / steps
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(start.elapsed_time(stop), world, dev)
     ms_step = ms_total / steps
     total_bytes = kv_bytes * world
-    value = total_bytes * steps / (ms_total * 1e-3) / 1e9
+    value = whole_job_gbps(kv_bytes, world, steps, ms_total)
 
     # end to end through the public API: pinned host inputs in, output back, every step
     e2e = None
@@ -403,11 +419,7 @@ def run_gb300(args):
             h_out.copy_(out.view(torch.int16), non_blocking=True)
         s1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = s0.elapsed_time(s1) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1) / e2e_steps, world, dev)
         e2e = {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,

@@ -6,7 +6,7 @@ namespace pa {
 
 cudaError_t launch_attn_group_d64(const CUtensorMap& tk, const CUtensorMap& tv,
                                   const AttnParams& p, int rows, dim3 grid, cudaStream_t s) {
-  return launch_dispatch<64, true>(tk, tv, p, rows, grid, s);
+  return launch_dispatch<64, true>(tk, tv, p, rows, grid, s, false);
 }
 
 cudaError_t take_error_group_d64(unsigned* bits) { return take_error_word(bits); }

@@ -52,7 +52,7 @@ struct Plan {
   int ppb = 1;           // pages per partition
   int max_parts = 1;     // partition slots per query row
   size_t ws_bytes = 0;   // scratch needed
-  size_t off_m = 0, off_l = 0;
+  size_t off_ml = 0;
 };
 
 // Partition sizes measured best on GB300: contexts up to 4096 tokens in
@@ -64,7 +64,7 @@ int default_partition_tokens(int max_context_len) {
   return ceil_div(max_context_len, kBlockSize) * kBlockSize;
 }
 
-// Scratch layout: [O partials][m][l], each region 256-byte aligned.
+// Scratch layout: [O partials][(m, l) pairs], each region 256-byte aligned.
 Plan make_plan(int num_seqs, int hq, int T, int max_ctx, int head_dim, int partition_size,
                int max_prefix_blocks) {
   Plan pl;
@@ -76,10 +76,9 @@ Plan make_plan(int num_seqs, int hq, int T, int max_ctx, int head_dim, int parti
   if (pl.max_parts == 1 && max_prefix_blocks == 0) return pl;   // no scratch
   const size_t rows = static_cast<size_t>(num_seqs) * T * hq;
   const size_t po = round256(rows * pl.max_parts * head_dim * sizeof(float));
-  const size_t pm = round256(rows * pl.max_parts * sizeof(float));
-  pl.off_m = po;
-  pl.off_l = po + pm;
-  pl.ws_bytes = po + 2 * pm;
+  const size_t pm = round256(rows * pl.max_parts * 2 * sizeof(float));
+  pl.off_ml = po;
+  pl.ws_bytes = po + pm;
   return pl;
 }
 
@@ -166,8 +165,7 @@ pa_status run_attention(const AttnArgs& a) {
   if (plan.ws_bytes > 0) {
     char* ws = static_cast<char*>(a.workspace);
     p.part_o = reinterpret_cast<float*>(ws);
-    p.part_m = reinterpret_cast<float*>(ws + plan.off_m);
-    p.part_l = reinterpret_cast<float*>(ws + plan.off_l);
+    p.part_ml = reinterpret_cast<float2*>(ws + plan.off_ml);
   }
   if (a.new_k != nullptr) {
     if (!a.new_v || !aligned16(a.new_k) || !aligned16(a.new_v)) return PA_ERR_INVALID_ARG;
@@ -194,7 +192,8 @@ pa_status run_attention(const AttnArgs& a) {
 
   const int max_blocks = ceil_div(a.max_context_len, kBlockSize);
   cudaError_t e = cudaSuccess;
-  if (grouped && a.max_prefix_blocks > 0) {
+  const bool group_launch = grouped && a.max_prefix_blocks > 0;
+  if (group_launch) {
     const int mc = std::min(a.max_group_size, kMaxRows / (G * a.T));
     p.members_per_chunk = mc;
     p.num_chunks = ceil_div(a.max_group_size, mc);
@@ -213,8 +212,8 @@ pa_status run_attention(const AttnArgs& a) {
                             a.num_seqs;
     if (units >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(units), 1, 1);
-    e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream)
-                         : launch_attn_d128(tk, tv, p, rows, grid, a.stream);
+    e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
+                         : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (plan.ws_bytes > 0) {

@@ -102,6 +102,14 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   __shared__ int s_nmem;
   __shared__ int s_bad;
 
+  if constexpr (GROUP) {
+    // The per-sequence kernel of the same call may run alongside this one.
+    grid_launch_dependents();
+  } else if (blockIdx.x == gridDim.x - 1) {
+    // When launched alongside a shared-prefix kernel, this grid must not
+    // complete before it (the split-KV merge that follows reads both).
+    grid_dependency_wait();
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Per-sequence mode: a 1-D grid in partition-major order (every sequence's
@@ -560,8 +568,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       const size_t pidx = orow * p.max_parts + slot;
       reinterpret_cast<float2*>(p.part_o)[(pidx * D + d) >> 1] = make_float2(o0 * inv, o1 * inv);
       if (d == 0) {
-        p.part_m[pidx] = M;
-        p.part_l[pidx] = Ls;
+        p.part_ml[pidx] = make_float2(M, Ls);
       }
     }
   }
@@ -569,7 +576,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 
 template <int D, class C, bool GROUP>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                       dim3 grid, cudaStream_t s) {
+                       dim3 grid, cudaStream_t s, bool overlap_previous) {
   constexpr int smem = Smem<D, C::NT, C::NTW>::kAlloc;
   auto kern = paged_attn_kernel<D, C, GROUP>;
   static int configured_device = -1;         // attribute set once per device in practice
@@ -581,21 +588,36 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const AttnP
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  kern<<<grid, C::kThreads, smem, s>>>(tk, tv, p);
-  return cudaGetLastError();
+  if (!overlap_previous) {
+    kern<<<grid, C::kThreads, smem, s>>>(tk, tv, p);
+    return cudaGetLastError();
+  }
+  // Programmatic stream serialisation: may start while the previous kernel runs.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 // `rows` = query rows per CTA (1..64).  One n-tile per warp keeps registers low
 // and many warps resident (latency hiding); warp columns split the rows.
 template <int D, bool GROUP>
 cudaError_t launch_dispatch(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                            int rows, dim3 grid, cudaStream_t s) {
+                            int rows, dim3 grid, cudaStream_t s, bool overlap_previous) {
+  const bool o = overlap_previous;
   if (rows <= 0) return cudaErrorInvalidValue;
-  if (rows <= 8) return launch_one<D, Cfg<1, 1, 4, 3>, GROUP>(tk, tv, p, grid, s);
-  if (rows <= 16) return launch_one<D, Cfg<1, 2, 2, 3>, GROUP>(tk, tv, p, grid, s);
-  if (rows <= 24) return launch_one<D, Cfg<1, 3, 2, 3>, GROUP>(tk, tv, p, grid, s);
-  if (rows <= 32) return launch_one<D, Cfg<1, 4, 2, 2>, GROUP>(tk, tv, p, grid, s);
-  if (rows <= 64) return launch_one<D, Cfg<2, 4, 1, 2>, GROUP>(tk, tv, p, grid, s);
+  if (rows <= 8) return launch_one<D, Cfg<1, 1, 4, 3>, GROUP>(tk, tv, p, grid, s, o);
+  if (rows <= 16) return launch_one<D, Cfg<1, 2, 2, 3>, GROUP>(tk, tv, p, grid, s, o);
+  if (rows <= 24) return launch_one<D, Cfg<1, 3, 2, 3>, GROUP>(tk, tv, p, grid, s, o);
+  if (rows <= 32) return launch_one<D, Cfg<1, 4, 2, 2>, GROUP>(tk, tv, p, grid, s, o);
+  if (rows <= 64) return launch_one<D, Cfg<2, 4, 1, 2>, GROUP>(tk, tv, p, grid, s, o);
   return cudaErrorInvalidValue;
 }
 

@@ -28,8 +28,8 @@ struct AttnParams {
   void* k_pool;                   // the pools again, for those writes
   void* v_pool;
   float* part_o;                  // [B*T*Hq, max_parts, D]   (split-KV partials)
-  float* part_m;                  // [B*T*Hq, max_parts]      running max, log2 domain
-  float* part_l;                  // [B*T*Hq, max_parts]      softmax denominator
+  float2* part_ml;                // [B*T*Hq, max_parts]      (reference max in the log2
+                                  //   domain, softmax denominator) per partition
   const int32_t* seq_group;       // [B] or nullptr
   const int32_t* group_prefix_blocks;  // [num_groups] or nullptr
   int mbs;                        // max_blocks_per_seq
@@ -46,10 +46,12 @@ struct AttnParams {
 
 // Kernel launchers (one translation unit per head_dim and mode); `rows` is the
 // number of query rows one CTA carries (1 .. kMaxRows).
+// overlap_previous: launch with programmatic stream serialisation so the kernel may
+// run alongside the shared-prefix kernel launched just before it.
 cudaError_t launch_attn_d64(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                            int rows, dim3 grid, cudaStream_t s);
+                            int rows, dim3 grid, cudaStream_t s, bool overlap_previous);
 cudaError_t launch_attn_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                             int rows, dim3 grid, cudaStream_t s);
+                             int rows, dim3 grid, cudaStream_t s, bool overlap_previous);
 cudaError_t launch_attn_group_d64(const CUtensorMap& tk, const CUtensorMap& tv,
                                   const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_group_d128(const CUtensorMap& tk, const CUtensorMap& tv,

@@ -49,29 +49,33 @@ cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, vo
 }
 
 // ---------------------------------------------------------------- split-KV merge
-// One CTA per (sequence b, kv head g, chunk of RB query rows); the rows of
-// (b, g) are its G*T query rows (the q heads that read kv head g, times the
-// query tokens).  Partition i of a row holds O_i (normalised), m_i (reference
-// max, log2 domain) and l_i (sum of 2^(s - m_i)); the merged row is
-// sum_i w_i O_i / sum_i w_i with w_i = l_i 2^(m_i - M), M = max_i m_i.
-// Phase 1 loads every (row, partition) statistic of the CTA at once and turns
-// it into a weight; phase 2 gives each thread 4 head dims of one row and sums
-// the partial rows with independent 16-byte loads.  Sequences that fit in one
-// partition were written by the attention kernel directly and are skipped
-// (same predicate).
-constexpr int kMergeThreads = 128;
-constexpr int kMergeMaxWeights = kMaxPartitions;   // rows x partitions per pass
+// W warps per query row (W = 1, 2 or 4; 4/W rows per 128-thread CTA).  The
+// rows of (sequence b, kv head g) are its G*T query rows (the q heads that read
+// kv head g, times the query tokens).  Partition i of a row holds O_i
+// (normalised) and (m_i, l_i): reference max in the log2 domain and sum of
+// 2^(s - m_i).  The merged row is sum_i w_i O_i / sum_i w_i with
+// w_i = l_i 2^(m_i - M), M = max_i m_i.  Warp k of a row merges partitions
+// k, k + W, ... against its own max (lane j weighting partition j of each
+// block of 32, every lane summing its head dims with eight 16-byte loads in
+// flight); the W partial merges are then combined by the same rule.
+// Sequences that fit in one partition were written by the attention kernel
+// directly and are skipped (same predicate).
+constexpr int kMergeWarps = 4;
 
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) splitkv_reduce_kernel(const AttnParams p) {
-  constexpr int C4 = D / 4;                   // float4 chunks per row
-  constexpr int RB = kMergeThreads / C4;      // rows per CTA: 4 (D 128) or 8 (D 64)
-  __shared__ float s_w[kMergeMaxWeights];
-  __shared__ float s_inv[RB];
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    splitkv_reduce_kernel(const AttnParams p, int warps_per_row) {
+  constexpr int DL = D / 32;                  // head dims per lane (4 or 2)
+  __shared__ float s_acc[kMergeWarps][D];
+  __shared__ float s_ms[kMergeWarps][2];
+  const int W = warps_per_row;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rows_per_cta = kMergeWarps / W;
   const int rows = p.G * p.T;
-  const int chunks = (rows + RB - 1) / RB;
+  const int chunks = (rows + rows_per_cta - 1) / rows_per_cta;
   const int bg = blockIdx.x / chunks;
-  const int r0 = (blockIdx.x % chunks) * RB;
+  const int r = (blockIdx.x % chunks) * rows_per_cta + warp / W;
+  const int sub = warp % W;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int L = p.context_lens[b];
   if (L < p.T || L > p.max_ctx) return;
@@ -81,73 +85,92 @@ __global__ void __launch_bounds__(kMergeThreads) splitkv_reduce_kernel(const Att
   const int nblk = (L + kBlockSize - 1) / kBlockSize;
   const int npre = (pre + p.ppb - 1) / p.ppb;
   const int nparts = npre + (nblk - pre + p.ppb - 1) / p.ppb;
-  if (pre == 0 && nparts == 1) return;
-  const int nr = min(RB, rows - r0);
+  if (pre == 0 && nparts == 1) return;       // uniform over the CTA
+  const bool live = r < rows;
   // row r = t * G + hl  ->  orow = (b*T + t)*Hq + g*G + hl
-  auto orow_of = [&](int r) {
-    return (static_cast<size_t>(b) * p.T + r / p.G) * p.Hq + g * p.G + r % p.G;
-  };
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kWarps = kMergeThreads / 32;
-  const int per_pass = max(1, min(nr, kMergeMaxWeights / nparts));
-  for (int q0 = 0; q0 < nr; q0 += per_pass) {
-    const int nq = min(per_pass, nr - q0);
-    __syncthreads();
-    // phase 1: m_i for every (row, partition) -> row max -> weights
-    for (int k = tid; k < nq * nparts; k += kMergeThreads)
-      s_w[k] = p.part_m[orow_of(r0 + q0 + k / nparts) * p.max_parts + k % nparts];
-    __syncthreads();
-    for (int r = warp; r < nq; r += kWarps) {
-      float M = -CUDART_INF_F;
-      for (int i = lane; i < nparts; i += 32) M = fmaxf(M, s_w[r * nparts + i]);
+  const size_t orow =
+      (static_cast<size_t>(b) * p.T + (live ? r : 0) / p.G) * p.Hq + g * p.G + (live ? r : 0) % p.G;
+  const float2* ml = p.part_ml + orow * p.max_parts;
+  const float* po = p.part_o + orow * p.max_parts * D + lane * DL;
+
+  // this warp's partitions: sub, sub + W, sub + 2W, ...
+  const int mine = live ? (nparts - sub + W - 1) / W : 0;
+  float M = -CUDART_INF_F;
+  for (int k = lane; k < mine; k += 32) M = fmaxf(M, ml[sub + k * W].x);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float S = 0.f;
-      for (int i = lane; i < nparts; i += 32) {
-        const float mi = s_w[r * nparts + i];
-        const float w = (mi == -CUDART_INF_F || M == -CUDART_INF_F)
-                            ? 0.f
-                            : p.part_l[orow_of(r0 + q0 + r) * p.max_parts + i] * exp2f(mi - M);
-        s_w[r * nparts + i] = w;
-        S += w;
-      }
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float S = 0.f, acc[DL];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-      if (lane == 0) s_inv[r] = S > 0.f ? 1.f / S : 0.f;
-    }
-    __syncthreads();
-    // phase 2: O = sum_i w_i O_i / S, 4 head dims per thread
-    const int r = tid / C4, c = tid % C4;
-    if (r < nq) {
-      const size_t orow = orow_of(r0 + q0 + r);
-      const float4* po = reinterpret_cast<const float4*>(p.part_o + orow * p.max_parts * D) + c;
-      const float* w = s_w + r * nparts;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < DL; ++k) acc[k] = 0.f;
+  for (int base = 0; base < mine; base += 32) {
+    // (m, l) of this lane's partition of the block (an L1 hit, loaded just above)
+    const float2 mlv = base + lane < mine ? ml[sub + (base + lane) * W]
+                                          : make_float2(-CUDART_INF_F, 0.f);
+    const float w = (mlv.x == -CUDART_INF_F || M == -CUDART_INF_F) ? 0.f
+                                                                  : mlv.y * exp2f(mlv.x - M);
+    S += w;
+    const int n = min(32, mine - base);
 #pragma unroll 8
-      for (int i = 0; i < nparts; ++i) {
-        const float4 x = po[static_cast<size_t>(i) * C4];
-        acc.x += w[i] * x.x;
-        acc.y += w[i] * x.y;
-        acc.z += w[i] * x.z;
-        acc.w += w[i] * x.w;
+    for (int k = 0; k < n; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      const float* src = po + static_cast<size_t>(sub + (base + k) * W) * D;
+      if constexpr (DL == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += wk * x.x;
+        acc[1] += wk * x.y;
+        acc[2] += wk * x.z;
+        acc[3] += wk * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += wk * x.x;
+        acc[1] += wk * x.y;
       }
-      const float inv = s_inv[r];
-      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(p.out) + (orow * D + 4 * c) / 2;
-      dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+
+  if (W > 1) {
+    // combine the W partial merges of the row: weights 2^(M_k - M_row)
+#pragma unroll
+    for (int k = 0; k < DL; ++k) s_acc[warp][lane * DL + k] = acc[k];
+    if (lane == 0) {
+      s_ms[warp][0] = M;
+      s_ms[warp][1] = S;
+    }
+    __syncthreads();
+    if (sub != 0 || !live) return;
+    float Mr = -CUDART_INF_F;
+    for (int k = 0; k < W; ++k) Mr = fmaxf(Mr, s_ms[warp + k][0]);
+    S = 0.f;
+#pragma unroll
+    for (int d = 0; d < DL; ++d) acc[d] = 0.f;
+    for (int k = 0; k < W; ++k) {
+      const float Mk = s_ms[warp + k][0];
+      const float f = (Mk == -CUDART_INF_F) ? 0.f : exp2f(Mk - Mr);
+      S += f * s_ms[warp + k][1];
+#pragma unroll
+      for (int d = 0; d < DL; ++d) acc[d] += f * s_acc[warp + k][lane * DL + d];
+    }
+  }
+  if (!live) return;
+  const float inv = S > 0.f ? 1.f / S : 0.f;
+  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(p.out) + (orow * D + lane * DL) / 2;
+#pragma unroll
+  for (int k = 0; k < DL; k += 2) dst[k / 2] = __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
 }
 
 cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s) {
-  const int rb = kMergeThreads / (head_dim / 4);
-  const long long chunks = (static_cast<long long>(p.G) * p.T + rb - 1) / rb;
+  // more warps per row when rows have many partitions (more loads in flight)
+  const int W = p.max_parts >= 32 ? 4 : (p.max_parts >= 12 ? 2 : 1);
+  const int rows_per_cta = kMergeWarps / W;
+  const long long chunks = (static_cast<long long>(p.G) * p.T + rows_per_cta - 1) / rows_per_cta;
   const long long ctas = static_cast<long long>(p.num_seqs) * p.Hkv * chunks;
   if (ctas == 0) return cudaSuccess;
   if (head_dim == 64)
-    splitkv_reduce_kernel<64><<<static_cast<unsigned>(ctas), kMergeThreads, 0, s>>>(p);
+    splitkv_reduce_kernel<64><<<static_cast<unsigned>(ctas), kMergeWarps * 32, 0, s>>>(p, W);
   else
-    splitkv_reduce_kernel<128><<<static_cast<unsigned>(ctas), kMergeThreads, 0, s>>>(p);
+    splitkv_reduce_kernel<128><<<static_cast<unsigned>(ctas), kMergeWarps * 32, 0, s>>>(p, W);
   return cudaGetLastError();
 }
 

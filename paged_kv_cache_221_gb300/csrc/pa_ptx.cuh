@@ -105,6 +105,19 @@ __device__ __forceinline__ float hw_exp2(float x) {
   return y;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Let the next kernel of the stream, if it was launched with programmatic
+// stream serialisation, start as soon as every CTA of this grid has started.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding kernel of the stream has completed and its writes
+// are visible (returns at once when there is no programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- named barrier
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
