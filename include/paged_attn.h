@@ -97,8 +97,9 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
 /*
  * pa_workspace_size — bytes of scratch the attention calls need for split-KV
  * partials with these sizes (0 if no sequence can need more than one
- * partition).  partition_size = 0 selects the library default, exactly as the
- * attention calls do.  max_prefix_blocks is 0 for pa_decode / pa_verify.
+ * partition).  With partition_size = 0 it sizes for the smallest partition the
+ * library default may pick (the default also depends on num_kv_heads), so the
+ * result always suffices.  max_prefix_blocks is 0 for pa_decode / pa_verify.
  */
 size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_query_tokens,
                          int max_context_len, int head_dim, int block_size, int partition_size,
@@ -123,9 +124,9 @@ int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_le
  * pa_workspace_size(...) bytes.  The workspace needs no initialisation (every
  * partial is written before it is read) and may be reused by later calls on
  * the same stream.  With partition_size = 0 and workspace == NULL every
- * sequence is processed whole (no scratch, fewer parallel units).  With an explicit
- * partition_size that needs scratch, a missing or short workspace returns
- * PA_ERR_WORKSPACE.
+ * sequence is processed whole (no scratch, fewer parallel units).  With an
+ * explicit partition_size that needs scratch, a missing or short workspace
+ * returns PA_ERR_WORKSPACE.
  *
  * max_context_len must bound every context_lens[b] and be at most
  * max_blocks_per_seq*block_size; it sizes the launch without a device read.

@@ -55,13 +55,16 @@ struct Plan {
   size_t off_ml = 0;
 };
 
-// Partition sizes measured best on GB300: contexts up to 4096 tokens in
-// 1024-token partitions (64 pages per CTA), longer ones in 2048-token
-// partitions (fewer partials to merge); contexts up to 1024 tokens stay whole.
-int default_partition_tokens(int max_context_len) {
-  if (max_context_len > 4096) return 2048;
-  if (max_context_len > 1024) return 1024;
-  return ceil_div(max_context_len, kBlockSize) * kBlockSize;
+// Partition sizes measured best on GB300: contexts up to 1024 tokens stay
+// whole; up to 4096 tokens, 1536-token partitions; longer contexts, 2048-token
+// partitions, or 3072 when there are many (sequence, kv head) pairs (>= 1024)
+// so that fewer partials need merging.  num_kv_heads = 0 (unknown) gives the
+// smallest of these choices, so a workspace sized with it always suffices.
+int default_partition_tokens(int max_context_len, int num_seqs, int num_kv_heads) {
+  if (max_context_len <= 1024) return ceil_div(max_context_len, kBlockSize) * kBlockSize;
+  if (max_context_len <= 4096) return 1536;
+  if (num_kv_heads > 0 && static_cast<long long>(num_seqs) * num_kv_heads >= 1024) return 3072;
+  return 2048;
 }
 
 // Scratch layout: [O partials][(m, l) pairs], each region 256-byte aligned.
@@ -138,7 +141,7 @@ pa_status run_attention(const AttnArgs& a) {
 
   int psize = a.partition_size;
   if (psize == 0) {
-    psize = default_partition_tokens(a.max_context_len);
+    psize = default_partition_tokens(a.max_context_len, a.num_seqs, a.hkv);
     Plan probe = make_plan(a.num_seqs, a.hq, a.T, a.max_context_len, a.head_dim, psize,
                            max_prefix);
     if (!grouped && probe.ws_bytes > 0 && a.workspace == nullptr)
@@ -262,11 +265,9 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
 
 int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_len,
                               int block_size) {
-  (void)num_seqs;
-  (void)num_kv_heads;
   (void)block_size;
   if (max_context_len < 1) return kBlockSize;
-  return default_partition_tokens(max_context_len);
+  return default_partition_tokens(max_context_len, num_seqs, num_kv_heads);
 }
 
 size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_query_tokens,
@@ -275,7 +276,8 @@ size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_query_tokens,
   if (num_seqs <= 0 || num_q_heads <= 0 || num_query_tokens <= 0 || max_context_len <= 0 ||
       head_dim <= 0 || block_size != kBlockSize || partition_size < 0 || max_prefix_blocks < 0)
     return 0;
-  const int psize = partition_size == 0 ? default_partition_tokens(max_context_len)
+  // num_kv_heads is not known here: size for the smallest default partition
+  const int psize = partition_size == 0 ? default_partition_tokens(max_context_len, num_seqs, 0)
                                         : partition_size;
   return make_plan(num_seqs, num_q_heads, num_query_tokens, max_context_len, head_dim, psize,
                    max_prefix_blocks)

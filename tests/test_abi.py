@@ -48,14 +48,15 @@ def test_workspace_size_host_only(lib):
     def r256(x):
         return (x + 255) // 256 * 256
 
-    def want(slots):        # [O partials][m][l]
-        return r256(rows * slots * 128 * 4) + 2 * r256(rows * slots * 4)
+    def want(slots):        # [O partials][(m, l) pairs]
+        return r256(rows * slots * 128 * 4) + r256(rows * slots * 8)
 
     assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 512, 0) == want(8)
-    assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 0, 0) == want(4)   # default 1024
-    assert lib.pa_default_partition_size(64, 8, 4096, 16) == 1024
+    assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 0, 0) == want(3)   # default 1536
+    assert lib.pa_default_partition_size(64, 8, 4096, 16) == 1536
     assert lib.pa_default_partition_size(64, 8, 100, 16) == 112
-    assert lib.pa_default_partition_size(64, 8, 16384, 16) == 2048
+    assert lib.pa_default_partition_size(32, 8, 16384, 16) == 2048
+    assert lib.pa_default_partition_size(256, 8, 8192, 16) == 3072
     # shared prefix always needs scratch
     assert lib.pa_workspace_size(2, 4, 1, 64, 64, 16, 64, 2) > 0
 
