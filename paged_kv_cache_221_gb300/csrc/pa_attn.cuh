@@ -46,10 +46,13 @@ struct Geo {
 // Consumer-warp layout: NT n-tiles of 8 query rows per warp, NTW warp columns
 // (rows 8*NT*NTW per CTA), PL page lanes (warps of one column that split the
 // pages), and the CTAs per SM the register budget must allow.
-template <int NT_, int NTW_, int PL_, int MINB_>
+// TP: pages per softmax step of a consumer warp (2 needs at least four ring
+// stages per page lane: two in use, two in flight).
+template <int NT_, int NTW_, int PL_, int MINB_, int TP_ = 1>
 struct Cfg {
-  static constexpr int NT = NT_, NTW = NTW_, PL = PL_, MINB = MINB_;
+  static constexpr int NT = NT_, NTW = NTW_, PL = PL_, MINB = MINB_, TP = TP_;
   static constexpr int kThreads = (NTW * PL + 1) * 32;
+  static_assert(TP == 1 || (TP == 2 && kStages / PL >= 4), "ring too short for TP");
 };
 
 template <int D, int NT, int NTW>
@@ -367,28 +370,51 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   for (int j = 0; j < NT; ++j) minlim = min(minlim, min(lim0[j], lim1[j]));
   minlim = __reduce_min_sync(0xffffffffu, minlim);
 
-  for (int it = pl; it < npages; it += PL) {
-    const int s = it % kStages;
-    const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-    if (!aborted && !mbar_wait(&full[s], ph, p.timeout_ns)) aborted = true;
-    if (!aborted && stage_ok[s]) {
-      const uint32_t kb = smem_u32(stages + s * Gm::kStageBytes);
-      const uint32_t vb = kb + Gm::kPageBytes;
-      const int tok0 = (pg0 + it) * kBlockSize;
+  // Each step handles TP pages of this lane (it, it + PL, ...): one score tile
+  // per page, one softmax update over all of them, one P.V per page.
+  constexpr int TP = C::TP;
+  for (int it = pl; it < npages; it += TP * PL) {
+    int nstep = 1;
+    if (TP == 2 && it + PL < npages) nstep = 2;
+    bool okp[TP];
+    uint32_t kb[TP], vb[TP];
+    int tok0[TP], sidx[TP];
+#pragma unroll
+    for (int k = 0; k < TP; ++k) {
+      okp[k] = false;
+      kb[k] = vb[k] = 0;
+      tok0[k] = sidx[k] = 0;
+      if (k < nstep) {
+        const int pg = it + k * PL;
+        const int s = pg % kStages;
+        const uint32_t ph = static_cast<uint32_t>(pg / kStages) & 1u;
+        if (!aborted && !mbar_wait(&full[s], ph, p.timeout_ns)) aborted = true;
+        okp[k] = !aborted && stage_ok[s];
+        sidx[k] = s;
+        kb[k] = smem_u32(stages + s * Gm::kStageBytes);
+        vb[k] = kb[k] + Gm::kPageBytes;
+        tok0[k] = (pg0 + pg) * kBlockSize;
+      }
+    }
 
-      // S^T[16 tokens x 8 rows] = K_page . Q^T per n-tile (two accumulation chains)
-      float sa[NT][4], sb[NT][4];
+    // S^T[16 tokens x 8 rows] = K_page . Q^T per page and n-tile (two chains each)
+    float sa[TP][NT][4], sb[TP][NT][4];
+#pragma unroll
+    for (int k = 0; k < TP; ++k)
 #pragma unroll
       for (int j = 0; j < NT; ++j)
-        sa[j][0] = sa[j][1] = sa[j][2] = sa[j][3] = sb[j][0] = sb[j][1] = sb[j][2] =
-            sb[j][3] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[k][j][e] = sb[k][j][e] = 0.f;
+#pragma unroll
+    for (int k = 0; k < TP; ++k) {
+      if (!okp[k]) continue;
 #pragma unroll
       for (int k2 = 0; k2 < Gm::kKSteps; k2 += 2) {
         uint32_t a[2][4];
         ldsm_x4(a[0][0], a[0][1], a[0][2], a[0][3],
-                kb + (k2 >> 2) * Gm::kHalfBytes + koff[k2 & 3]);
+                kb[k] + (k2 >> 2) * Gm::kHalfBytes + koff[k2 & 3]);
         ldsm_x4(a[1][0], a[1][1], a[1][2], a[1][3],
-                kb + ((k2 + 1) >> 2) * Gm::kHalfBytes + koff[(k2 + 1) & 3]);
+                kb[k] + ((k2 + 1) >> 2) * Gm::kHalfBytes + koff[(k2 + 1) & 3]);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           uint32_t b00, b01, b10, b11;
@@ -401,68 +427,85 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
             ldsm_x4(b00, b01, b10, b11,
                     qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + k2 * 32));
           }
-          mma_bf16_16816(sa[j], a[0][0], a[0][1], a[0][2], a[0][3], b00, b01);
-          mma_bf16_16816(sb[j], a[1][0], a[1][1], a[1][2], a[1][3], b10, b11);
+          mma_bf16_16816(sa[k][j], a[0][0], a[0][1], a[0][2], a[0][3], b00, b01);
+          mma_bf16_16816(sb[k][j], a[1][0], a[1][1], a[1][2], a[1][3], b10, b11);
         }
       }
+    }
 
-      // V rows at or past the context end may hold anything (even NaN): their
-      // weight is 0, but 0 * NaN is NaN, so zero them in the operand.
-      const int nvalid = vlen - tok0;
-      const bool interior = (tok0 + kBlockSize - 1 <= minlim) && (nvalid >= kBlockSize);
-      uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-      if (nvalid < kBlockSize) {
-        mlo = (2 * q4 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < nvalid ? 0xffff0000u : 0u);
-        mhi = (2 * q4 + 8 < nvalid ? 0x0000ffffu : 0u) |
-              (2 * q4 + 9 < nvalid ? 0xffff0000u : 0u);
+    // V rows at or past the context end may hold anything (even NaN): their
+    // weight is 0, but 0 * NaN is NaN, so zero them in the operand.
+    int nvalid[TP];
+    bool interior[TP];
+    uint32_t mlo[TP], mhi[TP];
+#pragma unroll
+    for (int k = 0; k < TP; ++k) {
+      nvalid[k] = vlen - tok0[k];
+      interior[k] = okp[k] && (tok0[k] + kBlockSize - 1 <= minlim) && (nvalid[k] >= kBlockSize);
+      mlo[k] = mhi[k] = 0xffffffffu;
+      if (nvalid[k] < kBlockSize) {
+        const int nv = nvalid[k];
+        mlo[k] = (2 * q4 < nv ? 0x0000ffffu : 0u) | (2 * q4 + 1 < nv ? 0xffff0000u : 0u);
+        mhi[k] = (2 * q4 + 8 < nv ? 0x0000ffffu : 0u) | (2 * q4 + 9 < nv ? 0xffff0000u : 0u);
+      }
+    }
+
+    uint32_t bh0[TP][NT], bh1[TP][NT], bl0[TP][NT], bl1[TP][NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      // lane holds S^T[j0][n], S^T[j0][n+1], S^T[j0+8][n], S^T[j0+8][n+1] of each
+      // page, n = rbase + 8j + 2q4 (t[k][0..3] in that order)
+      float t[TP][4];
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+      for (int k = 0; k < TP; ++k) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) t[k][e] = (sa[k][j][e] + sb[k][j][e]) * sl2;
+        if (!okp[k]) {
+          t[k][0] = t[k][1] = t[k][2] = t[k][3] = -CUDART_INF_F;
+        } else if (!interior[k]) {
+          const int j0 = tok0[k] + gid, j1 = j0 + 8;
+          t[k][0] = (j0 <= lim0[j]) ? t[k][0] : -CUDART_INF_F;
+          t[k][1] = (j0 <= lim1[j]) ? t[k][1] : -CUDART_INF_F;
+          t[k][2] = (j1 <= lim0[j]) ? t[k][2] : -CUDART_INF_F;
+          t[k][3] = (j1 <= lim1[j]) ? t[k][3] : -CUDART_INF_F;
+        }
+        mx0 = fmaxf(mx0, fmaxf(t[k][0], t[k][2]));
+        mx1 = fmaxf(mx1, fmaxf(t[k][1], t[k][3]));
       }
 
-      uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
-      const int j0 = tok0 + gid, j1 = j0 + 8;
+      // online softmax (log2 domain), statistics per row.  The reference max m
+      // only moves when a score exceeds it by more than 8 (so every weight
+      // 2^(t - m) stays <= 256); the accumulators are rescaled only then.
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        // lane holds S^T[j0][n], S^T[j0][n+1], S^T[j0+8][n], S^T[j0+8][n+1], n = rbase+8j+2q4
-        float t0 = (sa[j][0] + sb[j][0]) * sl2, t1 = (sa[j][1] + sb[j][1]) * sl2;
-        float t2 = (sa[j][2] + sb[j][2]) * sl2, t3 = (sa[j][3] + sb[j][3]) * sl2;
-        if (!interior) {
-          t0 = (j0 <= lim0[j]) ? t0 : -CUDART_INF_F;
-          t1 = (j0 <= lim1[j]) ? t1 : -CUDART_INF_F;
-          t2 = (j1 <= lim0[j]) ? t2 : -CUDART_INF_F;
-          t3 = (j1 <= lim1[j]) ? t3 : -CUDART_INF_F;
-        }
-
-        // online softmax (log2 domain), statistics per row.  The reference max m
-        // only moves when a score exceeds it by more than 8 (so every weight
-        // 2^(t - m) stays <= 256); the accumulators are rescaled only then.
-        float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const bool up0 = mx0 > m0[j] + 8.f, up1 = mx1 > m1[j] + 8.f;
+      if (__any_sync(0xffffffffu, up0 || up1)) {
+        const float al0 = up0 ? hw_exp2(m0[j] - mx0) : 1.f;
+        const float al1 = up1 ? hw_exp2(m1[j] - mx1) : 1.f;
+        if (up0) m0[j] = mx0;
+        if (up1) m1[j] = mx1;
+        l0[j] *= al0;
+        l1[j] *= al1;
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+          acc[j][mt][0] *= al0;
+          acc[j][mt][1] *= al1;
+          acc[j][mt][2] *= al0;
+          acc[j][mt][3] *= al1;
         }
-        const bool up0 = mx0 > m0[j] + 8.f, up1 = mx1 > m1[j] + 8.f;
-        if (__any_sync(0xffffffffu, up0 || up1)) {
-          const float al0 = up0 ? hw_exp2(m0[j] - mx0) : 1.f;
-          const float al1 = up1 ? hw_exp2(m1[j] - mx1) : 1.f;
-          if (up0) m0[j] = mx0;
-          if (up1) m1[j] = mx1;
-          l0[j] *= al0;
-          l1[j] *= al1;
+      }
+      const float mu0 = (m0[j] == -CUDART_INF_F) ? 0.f : m0[j];
+      const float mu1 = (m1[j] == -CUDART_INF_F) ? 0.f : m1[j];
 #pragma unroll
-          for (int mt = 0; mt < Gm::kKSteps; ++mt) {
-            acc[j][mt][0] *= al0;
-            acc[j][mt][1] *= al1;
-            acc[j][mt][2] *= al0;
-            acc[j][mt][3] *= al1;
-          }
-        }
-        const float mu0 = (m0[j] == -CUDART_INF_F) ? 0.f : m0[j];
-        const float mu1 = (m1[j] == -CUDART_INF_F) ? 0.f : m1[j];
-        const float p0 = hw_exp2(t0 - mu0), p1 = hw_exp2(t1 - mu1);
-        const float p2 = hw_exp2(t2 - mu0), p3 = hw_exp2(t3 - mu1);
+      for (int k = 0; k < TP; ++k) {
+        const float p0 = hw_exp2(t[k][0] - mu0), p1 = hw_exp2(t[k][1] - mu1);
+        const float p2 = hw_exp2(t[k][2] - mu0), p3 = hw_exp2(t[k][3] - mu1);
         l0[j] += p0 + p2;
         l1[j] += p1 + p3;
-
         // P^T as B operands: bf16 high part and bf16 residual, transposed 8x8 blocks
         const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
         const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
@@ -470,38 +513,46 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
         const float2 f23 = __bfloat1622float2(h23);
         const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
         const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
-        bh0[j] = movmatrix_trans(bf162_bits(h01));
-        bh1[j] = movmatrix_trans(bf162_bits(h23));
-        bl0[j] = movmatrix_trans(bf162_bits(r01));
-        bl1[j] = movmatrix_trans(bf162_bits(r23));
+        bh0[k][j] = movmatrix_trans(bf162_bits(h01));
+        bh1[k][j] = movmatrix_trans(bf162_bits(h23));
+        bl0[k][j] = movmatrix_trans(bf162_bits(r01));
+        bl1[k][j] = movmatrix_trans(bf162_bits(r23));
       }
+    }
 
-      // O^T[D x 8] += V_page^T . P^T per n-tile
+    // O^T[D x 8] += V_page^T . P^T per page and n-tile
+#pragma unroll
+    for (int k = 0; k < TP; ++k) {
+      if (!okp[k]) continue;
       auto pv = [&](auto tail) {
 #pragma unroll
         for (int mt = 0; mt < Gm::kKSteps; ++mt) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(a0, a1, a2, a3, vb + (mt >> 2) * Gm::kHalfBytes + voff[mt & 3]);
+          ldsm_x4_trans(a0, a1, a2, a3, vb[k] + (mt >> 2) * Gm::kHalfBytes + voff[mt & 3]);
           if constexpr (decltype(tail)::value) {
-            a0 &= mlo;
-            a1 &= mlo;
-            a2 &= mhi;
-            a3 &= mhi;
+            a0 &= mlo[k];
+            a1 &= mlo[k];
+            a2 &= mhi[k];
+            a3 &= mhi[k];
           }
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bh0[j], bh1[j]);
-            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bl0[j], bl1[j]);
+            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bh0[k][j], bh1[k][j]);
+            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bl0[k][j], bl1[k][j]);
           }
         }
       };
-      if (nvalid < kBlockSize)
+      if (nvalid[k] < kBlockSize)
         pv(std::true_type{});
       else
         pv(std::false_type{});
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < TP; ++k)
+        if (k < nstep) mbar_arrive(&empty[sidx[k]]);
+    }
   }
 
   // ------------------------------------------------------------------ merge + write
@@ -615,7 +666,7 @@ cudaError_t launch_dispatch(const CUtensorMap& tk, const CUtensorMap& tv, const 
   if (rows <= 0) return cudaErrorInvalidValue;
   if (rows <= 8) return launch_one<D, Cfg<1, 1, 4, 3>, GROUP>(tk, tv, p, grid, s, o);
   if (rows <= 16) return launch_one<D, Cfg<1, 2, 2, 3>, GROUP>(tk, tv, p, grid, s, o);
-  if (rows <= 24) return launch_one<D, Cfg<1, 3, 2, 3>, GROUP>(tk, tv, p, grid, s, o);
+  if (rows <= 24) return launch_one<D, Cfg<1, 3, 2, 2, 2>, GROUP>(tk, tv, p, grid, s, o);
   if (rows <= 32) return launch_one<D, Cfg<1, 4, 2, 2>, GROUP>(tk, tv, p, grid, s, o);
   if (rows <= 64) return launch_one<D, Cfg<2, 4, 1, 2>, GROUP>(tk, tv, p, grid, s, o);
   return cudaErrorInvalidValue;
