@@ -66,7 +66,8 @@ typedef enum {
   PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pa_workspace_size */
   PA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed                */
   PA_ERR_BOUNDS = 5,        /* device saw a block id / slot / length out of range  */
-  PA_ERR_TIMEOUT = 6        /* device pipeline wait exceeded its limit             */
+  PA_ERR_TIMEOUT = 6,       /* device pipeline wait exceeded its limit             */
+  PA_ERR_OUT_OF_BLOCKS = 7  /* block manager: no free physical block left          */
 } pa_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -237,6 +238,69 @@ pa_status pa_decode_static_scratch(void* out, const void* q, const void* k_cache
                                    int num_q_heads, int num_kv_heads, int head_dim,
                                    int block_size, float scale, int partition_size,
                                    pa_stream_t stream);
+
+/*
+ * pa_copy_blocks — copy whole physical blocks (every kv head, K and V pools)
+ * for copy-on-write: for each i, block block_pairs[2i] is copied onto block
+ * block_pairs[2i+1] (device int32 pairs), bits unchanged.  Used after
+ * pa_bm_append_slot reports a copy, before the new token is written.  A pair
+ * naming a block outside the pool sets PA_ERR_BOUNDS on the device and is
+ * skipped; a destination must not also be a source in the same call.
+ * Cited: "PagedAttention, ..." §1 (partage de mémoire, copie sur écriture);
+ * "LLM inference optimization: KV cache", §4.2.
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs,
+                         int num_pairs, int num_blocks, int num_kv_heads, int head_dim,
+                         int block_size, pa_stream_t stream);
+
+/*
+ * Block manager — host-side bookkeeping of the physical block pool (no device
+ * memory, no CUDA calls): sequences own ordered lists of physical blocks (their
+ * block tables); forked sequences share blocks through reference counts; the
+ * first write into a shared, partly filled block copies it (copy-on-write).
+ * Cited: "PagedAttention, ..." §1 (blocks placed anywhere, block table,
+ * partage de mémoire / copie sur écriture); "LLM inference optimization: KV
+ * cache", §4.1 (only the blocks needed are allocated), §4.2.
+ * Policy: a new block is always the lowest-numbered free block.  Not
+ * thread-safe.  Sequence ids are arbitrary ints.
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* A manager for num_blocks blocks of block_size tokens; *out receives it. */
+pa_status pa_bm_create(int num_blocks, int block_size, pa_block_manager** out);
+void pa_bm_destroy(pa_block_manager* bm);
+
+/* New sequence holding num_tokens tokens (ceil(num_tokens/block_size) fresh
+ * blocks).  PA_ERR_OUT_OF_BLOCKS (nothing changed) if too few are free;
+ * PA_ERR_INVALID_ARG if seq_id exists. */
+pa_status pa_bm_add_sequence(pa_block_manager* bm, int seq_id, int num_tokens);
+
+/* child_id shares every block of parent_id (reference counts + 1). */
+pa_status pa_bm_fork(pa_block_manager* bm, int parent_id, int child_id);
+
+/* Reserve the slot of the sequence's next token and count the token.  If the
+ * last block is full a fresh block is appended; if it is partly filled and
+ * shared, it is replaced by a fresh block and *copy_src -> *copy_dst names
+ * the copy to run (pa_copy_blocks) before writing; otherwise both are -1.
+ * *slot = physical_block*block_size + offset.  PA_ERR_OUT_OF_BLOCKS leaves the
+ * manager unchanged. */
+pa_status pa_bm_append_slot(pa_block_manager* bm, int seq_id, int64_t* slot, int32_t* copy_src,
+                            int32_t* copy_dst);
+
+/* Drop a sequence; blocks whose reference count reaches 0 become free. */
+pa_status pa_bm_free_sequence(pa_block_manager* bm, int seq_id);
+
+/* Host arrays: block_tables [num_seqs, max_blocks_per_seq] (-1 past the end)
+ * and context_lens [num_seqs] for the given sequences.  PA_ERR_INVALID_ARG if
+ * a sequence is unknown or holds more than max_blocks_per_seq blocks. */
+pa_status pa_bm_block_table(const pa_block_manager* bm, const int32_t* seq_ids, int num_seqs,
+                            int max_blocks_per_seq, int32_t* block_tables,
+                            int32_t* context_lens);
+
+/* Free blocks; reference count of a block; tokens of a sequence (-1: unknown). */
+int pa_bm_num_free_blocks(const pa_block_manager* bm);
+int pa_bm_ref_count(const pa_block_manager* bm, int block);
+int pa_bm_num_tokens(const pa_block_manager* bm, int seq_id);
 
 /*
  * pa_get_device_error — synchronise `stream`, then return and clear the sticky

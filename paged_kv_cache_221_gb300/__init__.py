@@ -28,7 +28,7 @@ from ._lib import PagedAttnError, STATUS_NAMES
 
 __all__ = ["reshape_and_cache", "decode", "verify", "decode_shared_prefix", "workspace_size",
            "default_partition_size", "get_device_error", "selftest_wait_timeout", "library",
-           "PagedAttnError", "STATUS_NAMES"]
+           "copy_blocks", "BlockManager", "PagedAttnError", "STATUS_NAMES"]
 
 
 def library() -> ctypes.CDLL:
@@ -231,3 +231,88 @@ def selftest_wait_timeout(timeout_ns: int, device=None) -> None:
         torch.device(device)
     _lib.check("pa_selftest_wait_timeout",
                library().pa_selftest_wait_timeout(int(timeout_ns), _stream(dev)))
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs) -> None:
+    """Copy whole physical blocks src -> dst in both pools (copy-on-write), bit-exact.
+
+    ``pairs``: sequence of (src, dst) ids or an int32 tensor [n, 2] (host or device).
+    """
+    _need("k_cache", k_cache, torch.bfloat16, 4)
+    dev = k_cache.device
+    _need("v_cache", v_cache, torch.bfloat16, 4, dev)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    t = pairs if isinstance(pairs, torch.Tensor) else torch.tensor(list(pairs), dtype=torch.int32)
+    t = t.to(device=dev, dtype=torch.int32).reshape(-1, 2).contiguous()
+    if t.shape[0] == 0:
+        return
+    NB, Hkv, BS, D = k_cache.shape
+    st = library().pa_copy_blocks(_vp(k_cache), _vp(v_cache), _vp(t), t.shape[0], NB, Hkv, D, BS,
+                                  _stream(dev))
+    _lib.check("pa_copy_blocks", st)
+
+
+class BlockManager:
+    """Host-side block manager of the paged KV cache (the library's native C++ manager).
+
+    Sequences own ordered lists of physical blocks; ``fork`` shares them; the
+    first append into a shared, partly filled block returns a copy to perform
+    (copy-on-write).  New blocks are the lowest-numbered free ones.
+    """
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        self._lib = library()
+        h = ctypes.c_void_p()
+        _lib.check("pa_bm_create", self._lib.pa_bm_create(num_blocks, block_size, ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_sequence(self, seq_id: int, num_tokens: int) -> None:
+        _lib.check("pa_bm_add_sequence", self._lib.pa_bm_add_sequence(self._h, seq_id, num_tokens))
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        _lib.check("pa_bm_fork", self._lib.pa_bm_fork(self._h, parent_id, child_id))
+
+    def append_slot(self, seq_id: int):
+        """Reserve the next token's slot: returns (slot, copy) with copy = (src, dst) or None."""
+        slot = ctypes.c_int64()
+        src, dst = ctypes.c_int32(), ctypes.c_int32()
+        _lib.check("pa_bm_append_slot", self._lib.pa_bm_append_slot(
+            self._h, seq_id, ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst)))
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def free_sequence(self, seq_id: int) -> None:
+        _lib.check("pa_bm_free_sequence", self._lib.pa_bm_free_sequence(self._h, seq_id))
+
+    def block_table(self, seq_ids, max_blocks_per_seq: int):
+        """(block_tables int32 [n, max_blocks], context_lens int32 [n]) as host tensors."""
+        ids = torch.tensor(list(seq_ids), dtype=torch.int32)
+        n = ids.numel()
+        tables = torch.empty((n, max_blocks_per_seq), dtype=torch.int32)
+        lens = torch.empty(n, dtype=torch.int32)
+        _lib.check("pa_bm_block_table", self._lib.pa_bm_block_table(
+            self._h, _vp(ids) if n else None, n, max_blocks_per_seq,
+            _vp(tables) if n else None, _vp(lens) if n else None))
+        return tables, lens
+
+    def num_free_blocks(self) -> int:
+        return int(self._lib.pa_bm_num_free_blocks(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return int(self._lib.pa_bm_ref_count(self._h, block))
+
+    def num_tokens(self, seq_id: int) -> int:
+        return int(self._lib.pa_bm_num_tokens(self._h, seq_id))

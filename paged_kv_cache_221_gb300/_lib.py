@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(HERE, "libpaged_attn.so")
 PA_OK = 0
 STATUS_NAMES = {
     0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
-    4: "PA_ERR_CUDA", 5: "PA_ERR_BOUNDS", 6: "PA_ERR_TIMEOUT",
+    4: "PA_ERR_CUDA", 5: "PA_ERR_BOUNDS", 6: "PA_ERR_TIMEOUT", 7: "PA_ERR_OUT_OF_BLOCKS",
 }
 
 # Every symbol the header declares, with (restype, argtypes).
@@ -35,6 +35,18 @@ SIGNATURES = {
                                      _i, _f, _i, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
     "pa_decode_static_scratch": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
                                       _i, _i, _f, _i, _vp]),
+    "pa_copy_blocks": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "pa_bm_create": (_i, [_i, _i, ctypes.POINTER(_vp)]),
+    "pa_bm_destroy": (None, [_vp]),
+    "pa_bm_add_sequence": (_i, [_vp, _i, _i]),
+    "pa_bm_fork": (_i, [_vp, _i, _i]),
+    "pa_bm_append_slot": (_i, [_vp, _i, ctypes.POINTER(ctypes.c_int64),
+                               ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
+    "pa_bm_free_sequence": (_i, [_vp, _i]),
+    "pa_bm_block_table": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
+    "pa_bm_num_free_blocks": (_i, [_vp]),
+    "pa_bm_ref_count": (_i, [_vp, _i]),
+    "pa_bm_num_tokens": (_i, [_vp, _i]),
     "pa_get_device_error": (_i, [_vp]),
     "pa_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
 }

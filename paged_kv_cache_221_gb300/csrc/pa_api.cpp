@@ -239,6 +239,7 @@ const char* pa_status_string(int status) {
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
     case PA_ERR_BOUNDS: return "PA_ERR_BOUNDS";
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+    case PA_ERR_OUT_OF_BLOCKS: return "PA_ERR_OUT_OF_BLOCKS";
     default: return "PA_ERR_UNKNOWN";
   }
 }
@@ -261,6 +262,23 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
       launch_reshape(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
                      num_kv_heads, head_dim, block_size, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs,
+                         int num_pairs, int num_blocks, int num_kv_heads, int head_dim,
+                         int block_size, pa_stream_t stream) {
+  if (num_pairs < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 != 0)
+    return PA_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (num_pairs > 65535) return PA_ERR_UNSUPPORTED;
+  if (!k_cache || !v_cache || !block_pairs || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  return launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs, num_blocks, num_kv_heads,
+                            head_dim, block_size, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_len,

@@ -60,6 +60,9 @@ cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_blocks, int hkv,
                            int head_dim, int block_size, cudaStream_t s);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                               int num_blocks, int hkv, int head_dim, int block_size,
+                               cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
 
 // Read and clear the device error word of each translation unit (synchronous).

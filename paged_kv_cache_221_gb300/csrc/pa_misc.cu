@@ -48,6 +48,40 @@ cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, vo
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- copy_blocks
+// Copy-on-write support: whole physical blocks (every kv head, K and V) are
+// copied from pairs[i][0] to pairs[i][1], bits unchanged.  Grid: (chunks of
+// one block, pair).  A pair naming a block outside the pool sets the BOUNDS
+// bit and is skipped.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       const int32_t* __restrict__ pairs, int num_blocks, long long vecs) {
+  const int src = pairs[2 * blockIdx.y], dst = pairs[2 * blockIdx.y + 1];
+  if (static_cast<unsigned>(src) >= static_cast<unsigned>(num_blocks) ||
+      static_cast<unsigned>(dst) >= static_cast<unsigned>(num_blocks)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_pa_err, kErrBounds);
+    return;
+  }
+  if (src == dst) return;
+  for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < vecs;
+       v += static_cast<long long>(gridDim.x) * blockDim.x) {
+    k_cache[dst * vecs + v] = k_cache[src * vecs + v];
+    v_cache[dst * vecs + v] = v_cache[src * vecs + v];
+  }
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
+                               int num_blocks, int hkv, int head_dim, int block_size,
+                               cudaStream_t s) {
+  if (num_pairs == 0) return cudaSuccess;
+  const long long vecs = static_cast<long long>(hkv) * block_size * head_dim / 8;
+  const long long chunks = (vecs + 255) / 256;
+  dim3 grid(static_cast<unsigned>(chunks < 64 ? chunks : 64), static_cast<unsigned>(num_pairs), 1);
+  copy_blocks_kernel<<<grid, 256, 0, s>>>(static_cast<uint4*>(k_cache),
+                                          static_cast<uint4*>(v_cache), pairs, num_blocks, vecs);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- split-KV merge
 // W warps per query row (W = 1, 2 or 4; 4/W rows per 128-thread CTA).  The
 // rows of (sequence b, kv head g) are its G*T query rows (the q heads that read
