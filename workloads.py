@@ -44,6 +44,7 @@ from typing import Optional
 import numpy as np
 
 NAN_BITS = np.uint16(0x7FC0)   # a quiet-NaN bf16 pattern used as the "never read" sentinel
+NAN_E4M3 = np.uint8(0x7F)       # the E4M3 NaN code, the same sentinel for FP8 pages
 BLOCK_SIZE = 16                 # tokens per physical block (the pages' example value)
 
 # Chunk size for random generation (elements); keeps temporaries near 256 MB.
@@ -92,6 +93,12 @@ class Workload:
     partition_size: int = 0         # tokens per split-KV partition (0 = library default)
     seq_group: Optional[np.ndarray] = None          # int32 [B], -1 = not in a group
     group_prefix_blocks: Optional[np.ndarray] = None  # int32 [num_groups]
+    # FP8 (E4M3) pages (``fp8_variant``): codes instead of bf16 pools, plus per-kv-head scales
+    kv_dtype: str = "bf16"
+    k_codes: Optional[np.ndarray] = None            # uint8 [NB, Hkv, BS, D]
+    v_codes: Optional[np.ndarray] = None            # uint8 [NB, Hkv, D, BS] (page transposed)
+    k_scale: Optional[np.ndarray] = None            # float32 [Hkv]
+    v_scale: Optional[np.ndarray] = None            # float32 [Hkv]
 
     @property
     def max_context_len(self) -> int:
@@ -135,8 +142,8 @@ class Workload:
         return int(nblk.sum()) * self.num_kv_heads
 
     def page_bytes(self) -> int:
-        """Bytes of one K page plus one V page (bf16)."""
-        return 2 * self.block_size * self.head_dim * 2
+        """Bytes of one K page plus one V page (2 bytes per value for bf16, 1 for fp8)."""
+        return 2 * self.block_size * self.head_dim * (1 if self.kv_dtype == "fp8" else 2)
 
     def kv_bytes(self) -> int:
         """Algorithmic KV bytes of one attention pass: unique pages x (K + V) page bytes."""
@@ -249,6 +256,45 @@ def build(name, context_lens, *, num_q_heads, num_kv_heads, head_dim, num_query_
                     slot_mapping=slots, scale=1.0 / math.sqrt(head_dim),
                     partition_size=partition_size, seq_group=seq_group,
                     group_prefix_blocks=group_prefix)
+
+
+def random_e4m3_codes(rng: np.random.Generator, shape, exp_lo=9, exp_hi=13) -> np.ndarray:
+    """Random E4M3 bit patterns: uniform sign bit, exponent field uniform in
+    [exp_lo, exp_hi], uniform 3-bit mantissa (no NaN code for exp_hi <= 14)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint8)
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        sign = rng.integers(0, 2, e - s, dtype=np.uint8)
+        ex = rng.integers(exp_lo, exp_hi + 1, e - s, dtype=np.uint8)
+        man = rng.integers(0, 8, e - s, dtype=np.uint8)
+        out[s:e] = (sign << np.uint8(7)) | (ex << np.uint8(3)) | man
+    return out.reshape(shape)
+
+
+def fp8_variant(w: Workload, seed: int = 0, scale_lo=1.0 / 96, scale_hi=1.0 / 48) -> Workload:
+    """The same workload with FP8 (E4M3) pages.
+
+    Same lengths, tables, queries, new tokens (bf16, still to be quantised by
+    reshape_and_cache) and slots.  Context slots hold random codes (exponent
+    field 9..13: magnitudes 4 .. 120 before scaling); every slot that holds
+    the bf16 sentinel in ``w`` (unused blocks, tails, the new tokens' slots)
+    holds the E4M3 NaN code.  Scales are one float32 per kv head, uniform in
+    [scale_lo, scale_hi].  V pages are stored transposed (``[D, BS]``).
+    """
+    rng = np.random.default_rng(seed + 5000)
+    NB, Hkv, BS, D = w.k_cache.shape
+    sentinel = w.k_cache[:, 0, :, 0] == NAN_BITS                   # [NB, BS]
+    k_codes = random_e4m3_codes(rng, (NB, Hkv, BS, D))
+    v_codes = random_e4m3_codes(rng, (NB, Hkv, D, BS))
+    blk, tok = np.nonzero(sentinel)
+    k_codes[blk, :, tok, :] = NAN_E4M3
+    v_codes[blk, :, :, tok] = NAN_E4M3
+    k_scale = rng.uniform(scale_lo, scale_hi, Hkv).astype(np.float32)
+    v_scale = rng.uniform(scale_lo, scale_hi, Hkv).astype(np.float32)
+    return dataclasses.replace(w, name=w.name + "_fp8", kv_dtype="fp8", k_cache=None,
+                               v_cache=None, k_codes=k_codes, v_codes=v_codes,
+                               k_scale=k_scale, v_scale=v_scale)
 
 
 # --------------------------------------------------------------------------
