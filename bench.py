@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="decode_8b")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="KV page format (fp8 = E4M3 pages with per-kv-head scales; the "
+                         "per-sequence path)")
     ap.add_argument("--partition-size", type=int, default=-1,
                     help="split-KV partition tokens (-1 = the workload's, 0 = library default)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -189,14 +192,26 @@ def cpu_baseline(workload, seconds):
 
 
 def workload_config(w, ps, world):
-    return {"workload": w.name, "desc": WORKLOAD_DESC.get(w.name, w.name),
+    base = w.name[:-4] if w.name.endswith("_fp8") else w.name
+    desc = WORKLOAD_DESC.get(base, base)
+    if w.kv_dtype == "fp8":
+        desc += "; FP8 (E4M3) K/V pages, per-kv-head scales, per-sequence path"
+    pool = (w.k_codes.nbytes + w.v_codes.nbytes) if w.kv_dtype == "fp8" else 2 * w.k_cache.nbytes
+    return {"workload": w.name, "desc": desc, "kv_dtype": w.kv_dtype,
             "num_seqs": w.num_seqs, "query_tokens": w.num_query_tokens,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": w.block_size, "pool_blocks": w.num_blocks,
             "partition_size": ps, "global_batch": w.num_seqs * world,
             "l2": "inputs larger than L2: each step reads %.2f GB of a %.2f GB pool (L2 129 MB)"
-                  % (w.kv_bytes() / 1e9, 2 * w.k_cache.nbytes / 1e9),
+                  % (w.kv_bytes() / 1e9, pool / 1e9),
             "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
+
+
+def data_desc(w):
+    if w.kv_dtype == "fp8":
+        return ("synthetic (seeded N(0,1) bf16 q and new K/V, random E4M3 codes in the pool, "
+                "random block placement)")
+    return "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)"
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -211,7 +226,7 @@ def run_reference(args):
     sys.path.insert(0, ROOT)
     from oracle import cpu_baseline as C
 
-    w, k, v = C.prepare(args.workload)
+    w, k, v = C.prepare(args.workload + ("_fp8" if args.kv_dtype == "fp8" else ""))
     # per-step sample: enough whole sequences for ~0.5 s, fewer when many steps are asked
     steps = args.steps if args.steps > 0 else 10
     per_seq = max(C.run_seqs(w, k, v, [0]), 1e-4)
@@ -239,7 +254,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
             "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)",
+            "data": data_desc(w),
             "config": workload_config(w, ps, 1),
             "seq_steps_per_s": round(nseq / dt, 3),
             "cpu_baseline": {"value": round(gbps, 4), "unit": "GB/s", "cores": C.threads_used(),
@@ -272,6 +287,12 @@ def run_gb300(args):
     import paged_kv_cache_221_gb300 as pa
 
     w = replica_workload(args.workload, rank)
+    fp8 = args.kv_dtype == "fp8"
+    if fp8:
+        import workloads as W
+        w.seq_group = None                  # FP8 pages run the per-sequence path
+        w.group_prefix_blocks = None
+        w = W.fp8_variant(w, seed=rank)
     ps = w.partition_size if args.partition_size < 0 else args.partition_size
 
     def td(a):
@@ -280,7 +301,9 @@ def run_gb300(args):
             t = t.view(torch.int16).view(torch.bfloat16)
         return t.to(dev)
 
-    q, k, v = td(w.q), td(w.k_cache), td(w.v_cache)
+    q = td(w.q)
+    k, v = (td(w.k_codes), td(w.v_codes)) if fp8 else (td(w.k_cache), td(w.v_cache))
+    ks, vs = (td(w.k_scale), td(w.v_scale)) if fp8 else (None, None)
     tables, lens = td(w.block_tables), td(w.context_lens)
     nk, nv, slots = td(w.new_key), td(w.new_value), td(w.slot_mapping)
     grouped = w.seq_group is not None
@@ -296,11 +319,15 @@ def run_gb300(args):
     # Per-sequence workloads: one fused call (reshape_and_cache inside the attention
     # launch).  Shared-prefix workload: reshape_and_cache, then the shared-prefix call.
     def reshape():
-        if grouped:
+        if fp8:
+            pa.reshape_and_cache_fp8(nk, nv, k, v, slots, ks, vs)
+        elif grouped:
             pa.reshape_and_cache(nk, nv, k, v, slots)
 
     def attend():
-        if grouped:
+        if fp8:
+            pa.verify_fp8(q, k, v, ks, vs, tables, lens, w.max_context_len, w.scale, ps, ws, out)
+        elif grouped:
             pa.decode_shared_prefix(q, k, v, tables, lens, sg, gp, w.max_group_size,
                                     w.max_prefix_blocks, w.max_context_len, w.scale, ps, ws, out)
         else:
@@ -308,7 +335,8 @@ def run_gb300(args):
                       nk, nv)
 
     # our kernels per step: attention (+ split-KV merge) (+ reshape + shared-prefix kernel)
-    launches_per_step = 1 + (1 if need > 0 else 0) + (2 if grouped else 0)
+    launches_per_step = 1 + (1 if need > 0 else 0) + (2 if grouped else 0) + (1 if fp8 else 0)
+    two_graphs = grouped or fp8
 
     stream = torch.cuda.current_stream(dev)
     # warm-up outside capture (sets kernel attributes), then capture one graph per phase
@@ -317,12 +345,12 @@ def run_gb300(args):
         attend()
     torch.cuda.synchronize(dev)
     assert pa.get_device_error(dev) == 0
-    g_reshape = torch.cuda.CUDAGraph() if grouped else None
+    g_reshape = torch.cuda.CUDAGraph() if two_graphs else None
     g_attend = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        if grouped:
+        if two_graphs:
             with torch.cuda.graph(g_reshape, stream=side):
                 reshape()
         with torch.cuda.graph(g_attend, stream=side):
@@ -437,27 +465,30 @@ def run_gb300(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 q/K/V, random block placement)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV / f16 MMA / fp32 softmax" if fp8 else "bf16",
+        "data": data_desc(w),
         "config": workload_config(w, ps, world),
         "seq_steps_per_s": round(w.num_seqs * world * steps / (ms_total * 1e-3), 1),
         "kv_bytes_per_step": kv_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(w.name),
+                     "traffic": None if fp8 else recorded_traffic(w.name),
                      "kernel": "attention call (paged_attn_kernel + splitkv_reduce_kernel)",
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "launch_ms_avg": round(attn_avg, 5),
                      "launch_ms_median": round(statistics.median(attn_ms), 5)},
         "clocks": clocks,
         "gpu_launches": launches_per_step * steps,
-        "timing": "CUDA graph of the step replayed (shared-prefix: reshape graph + attention "
-                  "graph); CUDA events on the launching stream around the attention call",
+        "timing": "CUDA graph of the step replayed (shared-prefix and FP8: reshape graph + "
+                  "attention graph); CUDA events on the launching stream around the attention "
+                  "call",
     }
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w.name, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload + ("_fp8" if fp8 else ""),
+                                            args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

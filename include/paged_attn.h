@@ -161,6 +161,64 @@ pa_status pa_verify(void* out, const void* q, const void* k_cache, const void* v
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * FP8 (E4M3) pages — the same cache with every K and V value stored as one
+ * byte, which halves the bytes decode streams ("ranksignal" post, Quantifier :
+ * des nombres plus petits: halving the precision halves what decode loads, FP8
+ * being the usual compromise, the softmax kept at full precision;
+ * "PagedAttention, ..." §3 on FP8).  Format: E4M3 without infinities (sign,
+ * 4-bit exponent with bias 7, 3-bit mantissa; exponent 0 = subnormals m*2^-9;
+ * 0x7F / 0xFF = NaN; largest magnitude 448).  Scales: k_scale[h], v_scale[h]
+ * (device float32 [num_kv_heads]) are chosen by the caller; a value x of kv
+ * head h is stored as the code nearest to x / scale[h] and read as
+ * value(code) * scale[h].  Layouts (uint8, each (block, kv head) page
+ * contiguous, block_size*head_dim bytes):
+ *   k_cache  [num_blocks, num_kv_heads, block_size, head_dim]   (token-major)
+ *   v_cache  [num_blocks, num_kv_heads, head_dim, block_size]   (transposed)
+ */
+
+/*
+ * pa_reshape_and_cache_fp8 — pa_reshape_and_cache into FP8 pages: for token i
+ * with s = slot_mapping[i] >= 0, block = s / block_size, t = s % block_size,
+ *   k_cache[block, h, t, d] = e4m3(key[i, h, d] / k_scale[h])
+ *   v_cache[block, h, d, t] = e4m3(value[i, h, d] / v_scale[h])
+ * where the division is IEEE float32 and e4m3() rounds to nearest even and
+ * saturates to +-448 (NaN stays NaN).  key/value are bf16 [num_tokens,
+ * num_kv_heads, head_dim].  Requirements and errors as pa_reshape_and_cache;
+ * k_scale and v_scale non-NULL.
+ */
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache,
+                                   void* v_cache, const int64_t* slot_mapping,
+                                   const float* k_scale, const float* v_scale, int num_tokens,
+                                   int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                                   pa_stream_t stream);
+
+/*
+ * pa_decode_fp8 / pa_verify_fp8 — pa_decode / pa_verify over FP8 pages: the
+ * same result with K_j = value(k code) * k_scale[h] and V_j = value(v code) *
+ * v_scale[h].  The products run on f16 operands with fp32 accumulation: q is
+ * converted to f16 (exact for |q| in [2^-14, 65504]; larger magnitudes are
+ * not supported, smaller ones lose the bits below 2^-24) and the softmax
+ * weights are rounded to f16 before they multiply V.  Workspace, partitions,
+ * requirements and errors as pa_decode / pa_verify, plus k_scale, v_scale
+ * non-NULL.
+ */
+pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens,
+                        int max_context_len, int num_seqs, int num_blocks, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, float scale,
+                        int partition_size, void* workspace, size_t workspace_bytes,
+                        pa_stream_t stream);
+
+pa_status pa_verify_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens,
+                        int max_context_len, int num_seqs, int num_query_tokens, int num_blocks,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        float scale, int partition_size, void* workspace,
+                        size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_append — reshape_and_cache fused into the attention call: the K
  * and V vectors of every sequence's num_query_tokens (T) query tokens,
  *   new_key, new_value  [num_seqs, T, num_kv_heads, head_dim]  bf16,

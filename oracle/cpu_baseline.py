@@ -7,7 +7,9 @@ BLAS thread count can be pinned before NumPy loads:
     OPENBLAS_NUM_THREADS=1 OMP_NUM_THREADS=1 python -m oracle.cpu_baseline decode_8b 10
 
 prints one JSON object: KV bytes read by the oracle (unique pages of the
-sequences it processed), seconds, GB/s and the sample description.  The
+sequences it processed), seconds, GB/s and the sample description.  A name
+ending in ``_fp8`` times the FP8-page oracle on that workload's FP8 variant
+(the per-sequence path, variant seed 0).  The
 workload's new tokens are scattered into the caches before timing; the timed
 work is the oracle's paged attention over whole sequences, in batch order,
 repeated over the batch until ``seconds`` have elapsed.
@@ -26,6 +28,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
+from oracle import fp8 as F  # noqa: E402
 from oracle import oracle as O  # noqa: E402
 
 
@@ -37,6 +40,14 @@ def threads_used() -> int:
 
 
 def prepare(name: str):
+    if name.endswith("_fp8"):
+        w = W.FULL[name[:-4]]()
+        w.seq_group = None
+        w.group_prefix_blocks = None
+        w = W.fp8_variant(w, seed=0)
+        k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
+                                   w.k_scale, w.v_scale, w.block_size)
+        return w, k, v
     w = W.FULL[name]()
     k, v = O.reshape_and_cache(w.new_key, w.new_value, w.k_cache, w.v_cache, w.slot_mapping,
                                w.block_size)
@@ -55,8 +66,12 @@ def run_seqs(w, k, v, seqs):
     """Oracle attention over exactly ``seqs``, one sequence at a time; returns seconds."""
     t0 = time.perf_counter()
     for b in seqs:
-        O.paged_attention(w.q, k, v, w.block_tables, w.context_lens, w.scale, w.num_kv_heads,
-                          w.block_size, seqs=[b])
+        if w.kv_dtype == "fp8":
+            F.paged_attention(w.q, k, v, w.k_scale, w.v_scale, w.block_tables, w.context_lens,
+                              w.scale, w.num_kv_heads, w.block_size, seqs=[b])
+        else:
+            O.paged_attention(w.q, k, v, w.block_tables, w.context_lens, w.scale,
+                              w.num_kv_heads, w.block_size, seqs=[b])
     return time.perf_counter() - t0
 
 

@@ -14,6 +14,12 @@ Layouts (bf16 unless stated):
     context_lens  [num_seqs] int32 (counts the newest token / the drafts)
     key, value    [num_tokens, num_kv_heads, head_dim]
     slot_mapping  [num_tokens] int64
+
+FP8 (E4M3) pages (``reshape_and_cache_fp8``, ``decode_fp8``, ``verify_fp8``):
+    k_cache       [num_blocks, num_kv_heads, block_size, head_dim] uint8 codes
+    v_cache       [num_blocks, num_kv_heads, head_dim, block_size] uint8 codes
+    k_scale,
+    v_scale       [num_kv_heads] float32 (value = code value * scale)
 """
 from __future__ import annotations
 
@@ -28,7 +34,8 @@ from ._lib import PagedAttnError, STATUS_NAMES
 
 __all__ = ["reshape_and_cache", "decode", "verify", "decode_shared_prefix", "workspace_size",
            "default_partition_size", "get_device_error", "selftest_wait_timeout", "library",
-           "copy_blocks", "BlockManager", "PagedAttnError", "STATUS_NAMES"]
+           "copy_blocks", "BlockManager", "reshape_and_cache_fp8", "decode_fp8", "verify_fp8",
+           "PagedAttnError", "STATUS_NAMES"]
 
 
 def library() -> ctypes.CDLL:
@@ -76,6 +83,88 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
     st = library().pa_reshape_and_cache(_vp(key), _vp(value), _vp(k_cache), _vp(v_cache),
                                         _vp(slot_mapping), N, NB, Hkv, D, BS, _stream(dev))
     _lib.check("pa_reshape_and_cache", st)
+
+
+def _fp8_pools(k_cache, v_cache, k_scale, v_scale):
+    _need("k_cache", k_cache, torch.uint8, 4)
+    dev = k_cache.device
+    _need("v_cache", v_cache, torch.uint8, 4, dev)
+    NB, Hkv, BS, D = k_cache.shape
+    if tuple(v_cache.shape) != (NB, Hkv, D, BS):
+        raise ValueError("v_cache must be [num_blocks, num_kv_heads, head_dim, block_size]")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _need(name, t, torch.float32, 1, dev)
+        if t.shape[0] != Hkv:
+            raise ValueError(f"{name} must have num_kv_heads entries")
+    return dev, NB, Hkv, BS, D
+
+
+def reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                          k_scale: torch.Tensor, v_scale: torch.Tensor) -> None:
+    """Quantise new bf16 K/V rows to E4M3 (value / scale) and store them in FP8 pages."""
+    dev, NB, Hkv, BS, D = _fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    _need("key", key, torch.bfloat16, 3, dev)
+    _need("value", value, torch.bfloat16, 3, dev)
+    _need("slot_mapping", slot_mapping, torch.int64, 1, dev)
+    N = key.shape[0]
+    if key.shape != (N, Hkv, D) or value.shape != key.shape or slot_mapping.shape[0] != N:
+        raise ValueError("inconsistent shapes")
+    st = library().pa_reshape_and_cache_fp8(_vp(key), _vp(value), _vp(k_cache), _vp(v_cache),
+                                            _vp(slot_mapping), _vp(k_scale), _vp(v_scale), N,
+                                            NB, Hkv, D, BS, _stream(dev))
+    _lib.check("pa_reshape_and_cache_fp8", st)
+
+
+def verify_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+               k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, max_context_len: Optional[int] = None,
+               scale: Optional[float] = None, partition_size: int = 0,
+               workspace: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """``verify`` (T >= 1 query tokens per sequence) over FP8 pages."""
+    dev, NB, Hkv, BS, D = _fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    _need("q", q, torch.bfloat16, 4, dev)
+    _need("block_tables", block_tables, torch.int32, 2, dev)
+    _need("context_lens", context_lens, torch.int32, 1, dev)
+    B, T, Hq, Dq = q.shape
+    if Dq != D or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("inconsistent shapes")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if B else T   # host sync
+    mcl = int(max_context_len)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need("out", out, torch.bfloat16, 4, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    need = workspace_size(B, Hq, T, mcl, D, BS, partition_size, 0) if B else 0
+    ws, wsb = _workspace(dev, workspace, need)
+    st = library().pa_verify_fp8(_vp(out), _vp(q), _vp(k_cache), _vp(v_cache), _vp(k_scale),
+                                 _vp(v_scale), _vp(block_tables), block_tables.shape[1],
+                                 _vp(context_lens), mcl, B, T, NB, Hq, Hkv, D, BS, scale,
+                                 partition_size, _vp(ws), wsb, _stream(dev))
+    _lib.check("pa_verify_fp8", st)
+    return out
+
+
+def decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+               k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, max_context_len: Optional[int] = None,
+               scale: Optional[float] = None, partition_size: int = 0,
+               workspace: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Single-token decode over FP8 pages; q is [B, Hq, D] or [B, 1, Hq, D]."""
+    squeeze = q.dim() == 3
+    q4 = q.unsqueeze(1) if squeeze else q
+    if q4.shape[1] != 1:
+        raise ValueError("decode_fp8 takes one query token per sequence (use verify_fp8)")
+    o4 = None if out is None else (out.unsqueeze(1) if squeeze else out)
+    r = verify_fp8(q4, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                   max_context_len, scale, partition_size, workspace, o4)
+    return r.squeeze(1) if squeeze else r
 
 
 def workspace_size(num_seqs: int, num_q_heads: int, num_query_tokens: int, max_context_len: int,

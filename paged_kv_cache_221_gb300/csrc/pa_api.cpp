@@ -42,6 +42,34 @@ bool encode_pool_map(CUtensorMap* map, const void* base, long long rows, int hea
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// FP8 pools.  K [num_blocks, Hkv, 16, D] bytes viewed as rows of D codes; one
+// 16 x D box per page (128-byte swizzle at D = 128, none at D = 64).  V
+// [num_blocks, Hkv, D, 16] bytes viewed as rows of 128 bytes; one box of D/8
+// rows per page, unswizzled.
+bool encode_fp8_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_base, const void* v_base,
+                     long long pages, int head_dim) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[2] = {1, 1};
+  cuuint64_t kdims[2] = {static_cast<cuuint64_t>(head_dim),
+                         static_cast<cuuint64_t>(pages * kBlockSize)};
+  cuuint64_t kstr[1] = {static_cast<cuuint64_t>(head_dim)};
+  cuuint32_t kbox[2] = {static_cast<cuuint32_t>(head_dim), static_cast<cuuint32_t>(kBlockSize)};
+  if (fn(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_base), kdims, kstr, kbox, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE,
+         head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  // V page bytes as rows of 128: one box of head_dim/8 rows (few long rows keep the
+  // TMA unit's per-row cost low; shared memory sees the same contiguous bytes).
+  cuuint64_t vdims[2] = {128, static_cast<cuuint64_t>(pages * head_dim / 8)};
+  cuuint64_t vstr[1] = {128};
+  cuuint32_t vbox[2] = {128, static_cast<cuuint32_t>(head_dim / 8)};
+  return fn(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_base), vdims, vstr, vbox,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -105,6 +133,9 @@ struct AttnArgs {
   void* workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
+  bool kv8 = false;                 // FP8 (E4M3) pages with per-kv-head scales
+  const float* k_scale = nullptr;
+  const float* v_scale = nullptr;
 };
 
 pa_status run_attention(const AttnArgs& a) {
@@ -130,6 +161,10 @@ pa_status run_attention(const AttnArgs& a) {
   const long long rows = static_cast<long long>(a.num_blocks) * a.hkv * kBlockSize;
   if (rows >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
   const bool grouped = a.num_groups > 0;
+  if (a.kv8) {
+    if (!a.k_scale || !a.v_scale) return PA_ERR_INVALID_ARG;
+    if (a.new_k != nullptr || grouped) return PA_ERR_UNSUPPORTED;
+  }
   if (grouped) {
     if (!a.seq_group || !a.group_prefix_blocks || a.max_group_size < 1 ||
         a.max_prefix_blocks < 0 ||
@@ -156,9 +191,14 @@ pa_status run_attention(const AttnArgs& a) {
   }
 
   CUtensorMap tk, tv;
-  if (!encode_pool_map(&tk, a.k_cache, rows, a.head_dim) ||
-      !encode_pool_map(&tv, a.v_cache, rows, a.head_dim))
+  if (a.kv8) {
+    if (!encode_fp8_maps(&tk, &tv, a.k_cache, a.v_cache,
+                         static_cast<long long>(a.num_blocks) * a.hkv, a.head_dim))
+      return PA_ERR_CUDA;
+  } else if (!encode_pool_map(&tk, a.k_cache, rows, a.head_dim) ||
+             !encode_pool_map(&tv, a.v_cache, rows, a.head_dim)) {
     return PA_ERR_CUDA;
+  }
 
   AttnParams p{};
   p.q = a.q;
@@ -178,6 +218,8 @@ pa_status run_attention(const AttnArgs& a) {
     p.v_pool = const_cast<void*>(a.v_cache);
   }
   p.seq_group = grouped ? a.seq_group : nullptr;
+  p.k_scale = a.kv8 ? a.k_scale : nullptr;
+  p.v_scale = a.kv8 ? a.v_scale : nullptr;
   p.group_prefix_blocks = grouped ? a.group_prefix_blocks : nullptr;
   p.mbs = a.max_blocks_per_seq;
   p.max_ctx = a.max_context_len;
@@ -215,8 +257,12 @@ pa_status run_attention(const AttnArgs& a) {
                             a.num_seqs;
     if (units >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(units), 1, 1);
-    e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
-                         : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);
+    if (a.kv8)
+      e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream)
+                           : launch_attn8_d128(tk, tv, p, rows, grid, a.stream);
+    else
+      e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
+                           : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (plan.ws_bytes > 0) {
@@ -261,6 +307,26 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
   const cudaError_t e =
       launch_reshape(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
                      num_kv_heads, head_dim, block_size, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_cache,
+                                   void* v_cache, const int64_t* slot_mapping,
+                                   const float* k_scale, const float* v_scale, int num_tokens,
+                                   int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                                   pa_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 ||
+      head_dim % 8 != 0)
+    return PA_ERR_INVALID_ARG;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping || !k_scale || !v_scale)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const cudaError_t e = launch_reshape_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale,
+                                           v_scale, num_tokens, num_blocks, num_kv_heads,
+                                           head_dim, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -329,6 +395,34 @@ pa_status pa_verify(void* out, const void* q, const void* k_cache, const void* v
   return run_attention(a);
 }
 
+pa_status pa_verify_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens,
+                        int max_context_len, int num_seqs, int num_query_tokens, int num_blocks,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        float scale, int partition_size, void* workspace,
+                        size_t workspace_bytes, pa_stream_t stream) {
+  AttnArgs a{out, q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+             context_lens, max_context_len, num_seqs, num_query_tokens, num_blocks,
+             num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_size, nullptr,
+             nullptr, 0, 0, 0, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), true, k_scale, v_scale};
+  return run_attention(a);
+}
+
+pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens,
+                        int max_context_len, int num_seqs, int num_blocks, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, float scale,
+                        int partition_size, void* workspace, size_t workspace_bytes,
+                        pa_stream_t stream) {
+  return pa_verify_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, num_seqs, 1,
+                       num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                       partition_size, workspace, workspace_bytes, stream);
+}
+
 pa_status pa_decode_append(void* out, const void* q, const void* new_key, const void* new_value,
                            void* k_cache, void* v_cache, const int32_t* block_tables,
                            int max_blocks_per_seq, const int32_t* context_lens,
@@ -369,7 +463,8 @@ pa_status pa_get_device_error(pa_stream_t stream) {
   unsigned bits = 0;
   if (take_error_attn_d64(&bits) != cudaSuccess || take_error_attn_d128(&bits) != cudaSuccess ||
       take_error_group_d64(&bits) != cudaSuccess ||
-      take_error_group_d128(&bits) != cudaSuccess || take_error_misc(&bits) != cudaSuccess)
+      take_error_group_d128(&bits) != cudaSuccess || take_error_attn8_d64(&bits) != cudaSuccess ||
+      take_error_attn8_d128(&bits) != cudaSuccess || take_error_misc(&bits) != cudaSuccess)
     return PA_ERR_CUDA;
   if (bits & kErrTimeout) return PA_ERR_TIMEOUT;
   if (bits & kErrBounds) return PA_ERR_BOUNDS;

@@ -20,6 +20,19 @@
 // CTA (1 .. 64) fill the N side in n-tiles of 8.  A consumer warp carries NT
 // n-tiles, so it reads each K/V page from shared memory once for up to 32 rows;
 // NTW warp columns split larger row sets, and PL page lanes split the pages.
+//
+// FP8 pages (KV8): K pages hold E4M3 codes token-major ([16][D] bytes), V pages
+// hold them transposed ([D][16] bytes), with one dequantisation scale per kv
+// head for K and for V.  Codes are widened to f16 in registers (exact) and the
+// products run on the f16 tensor-core path with fp32 accumulation: Q is
+// converted to f16 once per CTA (stored in shared memory in the head-dim order
+// of the K bytes), P is one f16 operand (11 significant bits),
+// the K scale folds into the softmax scale and the V scale into the output.
+// The contraction order inside a 16-wide k step is free, so the operands are
+// fed in the order the byte layout delivers them: K rows are fed in the token
+// order sigma (below) so that P^T lands in the B registers in the same order
+// as the transposed V bytes land in the A registers, and Q is fed in the same
+// head-dim order as the K bytes.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -31,12 +44,14 @@
 
 namespace pa {
 
-template <int D>
+template <int D, bool KV8 = false>
 struct Geo {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
-  static constexpr int kHalves = D / 64;                // 128-byte swizzle rows per token
-  static constexpr int kHalfBytes = kBlockSize * 128;   // one 16 x 64 bf16 TMA box
-  static constexpr int kPageBytes = kHalves * kHalfBytes;
+  static constexpr int kNS = KV8 ? 2 * kStages : kStages;   // ring stages (same ring bytes)
+  static constexpr int kIssueGroup = KV8 ? 8 : 4;            // pages the producer issues at once
+  static constexpr int kHalves = D / 64;                // bf16: 128-byte swizzle rows per token
+  static constexpr int kHalfBytes = kBlockSize * 128;   // bf16: one 16 x 64 TMA box
+  static constexpr int kPageBytes = kBlockSize * D * (KV8 ? 1 : 2);
   static constexpr int kStageBytes = 2 * kPageBytes;    // K page + V page
   static constexpr int kQStride = D + 8;                // bf16 per Q row in smem (conflict-free)
   static constexpr int kOStride = D + 4;                // floats per merge row (conflict-free)
@@ -52,23 +67,24 @@ template <int NT_, int NTW_, int PL_, int MINB_, int TP_ = 1>
 struct Cfg {
   static constexpr int NT = NT_, NTW = NTW_, PL = PL_, MINB = MINB_, TP = TP_;
   static constexpr int kThreads = (NTW * PL + 1) * 32;
-  static_assert(TP == 1 || (TP == 2 && kStages / PL >= 4), "ring too short for TP");
+  static_assert(TP == 1 || TP == 2, "one or two pages per softmax step");
 };
 
-template <int D, int NT, int NTW>
+template <int D, int NT, int NTW, bool KV8 = false>
 struct Smem {
+  using Gm = Geo<D, KV8>;
   static constexpr int kRows = 8 * NT * NTW;
   static constexpr int kStagesOff = 0;
-  static constexpr int kQOff = kStages * Geo<D>::kStageBytes;
-  static constexpr int kLimOff = kQOff + kRows * Geo<D>::kQStride * 2;
+  static constexpr int kQOff = Gm::kNS * Gm::kStageBytes;
+  static constexpr int kLimOff = kQOff + kRows * Gm::kQStride * 2;
   static constexpr int kBarOff = (kLimOff + kRows * 4 + 7) / 8 * 8;
-  static constexpr int kOkOff = kBarOff + 2 * kStages * 8;
-  static constexpr int kMemOff = kOkOff + kStages * 4;
+  static constexpr int kOkOff = kBarOff + 2 * Gm::kNS * 8;
+  static constexpr int kMemOff = kOkOff + Gm::kNS * 4;
   static constexpr int kBytes = kMemOff + kMaxRows * 4;
   static constexpr int kAlloc = kBytes + 1024;          // room to align the base to 1 KB
   // merge buffer of one (page lane, warp column): m[8NT], l[8NT], O[8NT][kOStride]
   // (reuses the stage ring once every page is consumed)
-  static constexpr int kMergeFloats = 16 * NT + 8 * NT * Geo<D>::kOStride;
+  static constexpr int kMergeFloats = 16 * NT + 8 * NT * Gm::kOStride;
 };
 
 // Byte offset of 16-byte chunk `ch` (of D/8) of token row `tok` inside one
@@ -79,18 +95,38 @@ __device__ __forceinline__ uint32_t page_off(int tok, int ch) {
                                (((ch & 7) ^ (tok & 7)) << 4));
 }
 
-template <int D, class C, bool GROUP>
+// FP8 K page: 16 rows of D bytes, one TMA box, 128-byte swizzle at D = 128
+// (16-byte chunk c of row r at chunk c ^ (r % 8)), unswizzled at D = 64.
+template <int D>
+__device__ __forceinline__ uint32_t page8_off(int tok, int ch) {
+  if constexpr (D == 128)
+    return static_cast<uint32_t>(tok * 128 + ((ch ^ (tok & 7)) << 4));
+  else
+    return static_cast<uint32_t>(tok * D + (ch << 4));
+}
+
+// FP8 score-tile row m holds token sigma(m): rows 0-7 tokens 0,1,4,5,8,9,12,13
+// and rows 8-15 tokens 2,3,6,7,10,11,14,15.  After the P^T transpose lane
+// (gid, q) then holds tokens 4q, 4q+1 in its first B register and 4q+2, 4q+3 in
+// its second, which is the order of bytes 4q .. 4q+3 of a transposed V row.
+__device__ __forceinline__ int sigma_row(int m) {
+  return 4 * ((m & 7) >> 1) + (m & 1) + 2 * (m >> 3);
+}
+
+template <int D, class C, bool GROUP, bool KV8>
 __global__ void __launch_bounds__(C::kThreads, C::MINB)
     paged_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
   constexpr int NT = C::NT, NTW = C::NTW, PL = C::PL;
   constexpr int NCW = NTW * PL;              // consumer warps
   constexpr int NCT = NCW * 32;              // consumer threads
-  using Gm = Geo<D>;
-  using Sm = Smem<D, NT, NTW>;
-  static_assert(kStages % PL == 0, "each stage is always consumed by the same page lane");
-  static_assert(PL * NTW * Sm::kMergeFloats * 4 <= kStages * Gm::kStageBytes,
+  using Gm = Geo<D, KV8>;
+  using Sm = Smem<D, NT, NTW, KV8>;
+  constexpr int NS = Gm::kNS;
+  static_assert(NS % PL == 0, "each stage is always consumed by the same page lane");
+  static_assert(PL * NTW * Sm::kMergeFloats * 4 <= NS * Gm::kStageBytes,
                 "merge buffers fit in the stage ring");
+  static_assert(C::TP == 1 || NS / PL >= 4, "ring too short for two pages per step");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -99,7 +135,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem + Sm::kQOff);
   int* lim = reinterpret_cast<int*>(smem + Sm::kLimOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + NS;
   int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOff);
   int* members = reinterpret_cast<int*>(smem + Sm::kMemOff);
   __shared__ int s_nmem;
@@ -208,7 +244,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     }
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NTW);
     }
@@ -218,43 +254,56 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 
   // ------------------------------------------------------------------ producer
   // Starts streaming pages at once; the consumers gather the query rows meanwhile.
+  // Pages are issued in groups of GP: lane j of the group waits for its own
+  // stage and issues its own page, so one pass of the loop puts GP pages in
+  // flight (the per-page cost of waiting and issuing is paid once per group).
   if (warp == NCW) {
+    constexpr int GP = Gm::kIssueGroup;
+    static_assert(GP >= 1 && GP <= NS && 32 % GP == 0, "issue group");
     bool aborted = false;
     for (int base = 0; base < npages; base += 32) {
       const int phys_l = base == 0 ? phys_first
                                    : ((base + lane < npages) ? __ldg(trow + pg0 + base + lane) : 0);
       const int cnt = min(32, npages - base);
-      for (int j = 0; j < cnt; ++j) {
-        const int phys = __shfl_sync(0xffffffffu, phys_l, j);
-        if constexpr (!GROUP) {
-          // Query tokens' K/V that land in this page are stored into the pool
-          // first (reshape_and_cache fused), then the page is read by TMA.
-          const int pos0 = (pg0 + base + j) * kBlockSize;
-          const int lo = max(vlen - T, pos0), hi = min(vlen - 1, pos0 + kBlockSize - 1);
-          if (p.new_k != nullptr && lo <= hi &&
-              static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks)) {
-            constexpr int CH = D / 8;           // 16-byte chunks per row
-            for (int pos = lo; pos <= hi; ++pos) {
-              const size_t src = (static_cast<size_t>(b_single) * T + (pos - (vlen - T))) * p.Hkv + g;
-              const size_t dst = (static_cast<size_t>(phys) * p.Hkv + g) * kBlockSize +
-                                 (pos & (kBlockSize - 1));
-              for (int c = lane; c < 2 * CH; c += 32) {
-                const bool isv = c >= CH;
-                const int cc = isv ? c - CH : c;
-                const uint4 v = reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + cc];
-                reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + cc] = v;
+      for (int j0 = 0; j0 < cnt; j0 += GP) {
+        const int jn = min(j0 + GP, cnt);
+        if constexpr (!GROUP && !KV8) {
+          // Query tokens' K/V that land in these pages are stored into the pool
+          // first (reshape_and_cache fused), then the pages are read by TMA.
+          if (p.new_k != nullptr) {
+            bool wrote = false;                 // warp-uniform
+            for (int j = j0; j < jn; ++j) {
+              const int phys = __shfl_sync(0xffffffffu, phys_l, j);
+              const int pos0 = (pg0 + base + j) * kBlockSize;
+              const int lo = max(vlen - T, pos0), hi = min(vlen - 1, pos0 + kBlockSize - 1);
+              if (lo > hi || static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks))
+                continue;
+              constexpr int CH = D / 8;         // 16-byte chunks per row
+              for (int pos = lo; pos <= hi; ++pos) {
+                const size_t src =
+                    (static_cast<size_t>(b_single) * T + (pos - (vlen - T))) * p.Hkv + g;
+                const size_t dst = (static_cast<size_t>(phys) * p.Hkv + g) * kBlockSize +
+                                   (pos & (kBlockSize - 1));
+                for (int c = lane; c < 2 * CH; c += 32) {
+                  const bool isv = c >= CH;
+                  const int cc = isv ? c - CH : c;
+                  const uint4 v =
+                      reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + cc];
+                  reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + cc] = v;
+                }
               }
+              wrote = true;
             }
-            fence_proxy_async_global();
+            if (wrote) fence_proxy_async_global();
             __syncwarp();
           }
         }
-        if (lane == 0) {
-          const int it = base + j;
-          const int s = it % kStages;
-          const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+        if (lane >= j0 && lane < jn) {
+          const int it = base + lane;
+          const int s = it % NS;
+          const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
           if (!aborted && !mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns)) aborted = true;
-          const bool ok = static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
+          const bool ok = static_cast<unsigned>(phys_l) < static_cast<unsigned>(p.num_blocks);
           if (!ok) atomicOr(&g_pa_err, kErrBounds);
           if (!ok || aborted) {
             stage_ok[s] = 0;
@@ -262,23 +311,31 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
           } else {
             stage_ok[s] = 1;
             mbar_arrive_expect_tx(&full[s], Gm::kStageBytes);
-            const int row = (phys * p.Hkv + g) * kBlockSize;
+            const int row = (phys_l * p.Hkv + g) * kBlockSize;
             uint8_t* st = stages + s * Gm::kStageBytes;
+            if constexpr (KV8) {
+              tma_load_2d(st, &tmk, &full[s], 0, row);                      // 16 x D codes
+              tma_load_2d(st + Gm::kPageBytes, &tmv, &full[s], 0,
+                          (phys_l * p.Hkv + g) * (D / 8));                   // D x 16 codes
+            } else {
 #pragma unroll
-            for (int h = 0; h < Gm::kHalves; ++h)
-              tma_load_2d(st + h * Gm::kHalfBytes, &tmk, &full[s], h * 64, row);
+              for (int h = 0; h < Gm::kHalves; ++h)
+                tma_load_2d(st + h * Gm::kHalfBytes, &tmk, &full[s], h * 64, row);
 #pragma unroll
-            for (int h = 0; h < Gm::kHalves; ++h)
-              tma_load_2d(st + Gm::kPageBytes + h * Gm::kHalfBytes, &tmv, &full[s], h * 64, row);
+              for (int h = 0; h < Gm::kHalves; ++h)
+                tma_load_2d(st + Gm::kPageBytes + h * Gm::kHalfBytes, &tmv, &full[s], h * 64,
+                            row);
+            }
           }
         }
-        __syncwarp();
+        // a wait that gave up on any lane ends the streaming of the whole warp
+        aborted = __any_sync(0xffffffffu, aborted);
       }
     }
     // Do not leave while copies issued by this warp may still be landing.
     if (lane == 0) {
-      for (int it = max(0, npages - kStages); it < npages; ++it)
-        mbar_wait(&full[it % kStages], static_cast<uint32_t>(it / kStages) & 1u, p.timeout_ns);
+      for (int it = max(0, npages - NS); it < npages; ++it)
+        mbar_wait(&full[it % NS], static_cast<uint32_t>(it / NS) & 1u, p.timeout_ns);
     }
     return;
   }
@@ -296,7 +353,19 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
         const size_t row = (static_cast<size_t>(b) * T + t) * p.Hq + g * G + hl;
         v = reinterpret_cast<const uint4*>(p.q)[row * CH + ch];
       }
-      *reinterpret_cast<uint4*>(qs + n * Gm::kQStride + ch * 8) = v;
+      if constexpr (KV8) {
+        // f16, and inside every 16 dims in the order of the FP8 K bytes: dims
+        // 4q, 4q+1 at positions 2q, 2q+1 and dims 4q+2, 4q+3 at 2q+8, 2q+9, so
+        // that the usual B-operand ldmatrix hands lane q the dims its K bytes hold.
+        uint32_t* dst = reinterpret_cast<uint32_t*>(qs + n * Gm::kQStride + (ch >> 1) * 16 +
+                                                    4 * (ch & 1));
+        dst[0] = bf16x2_to_f16x2(v.x);        // dims 8h, 8h+1      -> 4h, 4h+1
+        dst[4] = bf16x2_to_f16x2(v.y);        // dims 8h+2, 8h+3    -> 4h+8, 4h+9
+        dst[1] = bf16x2_to_f16x2(v.z);        // dims 8h+4, 8h+5    -> 4h+2, 4h+3
+        dst[5] = bf16x2_to_f16x2(v.w);        // dims 8h+6, 8h+7    -> 4h+10, 4h+11
+      } else {
+        *reinterpret_cast<uint4*>(qs + n * Gm::kQStride + ch * 8) = v;
+      }
     }
     for (int n = threadIdx.x; n < Sm::kRows; n += NCT) {
       // Padding rows (query 0) see every position: their columns of the tiles
@@ -317,7 +386,12 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   const int pl = warp / NTW;                 // page lane: pages pl, pl+PL, ...
   const int gid = lane >> 2, q4 = lane & 3;
   const int rbase = 8 * NT * col;
-  const float sl2 = p.scale_log2;
+  float sl2 = p.scale_log2;
+  float out_scale = 1.f;
+  if constexpr (KV8) {
+    sl2 *= p.k_scale[g];
+    out_scale = p.v_scale[g];
+  }
   int lim0[NT], lim1[NT];                    // this lane's rows rbase+8j+2q4 (+1)
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
@@ -360,9 +434,18 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   uint32_t koff[4], voff[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    koff[k] = page_off(ktok, 2 * k + kch);
-    voff[k] = page_off(vtok, 2 * k + vch);
+    if constexpr (KV8) {
+      // k: 16-byte chunk pair (2k, 2k+1) = head dims 32k .. 32k+31, rows fed as sigma
+      koff[k] = page8_off<D>(sigma_row(ktok), 2 * k + kch);
+      voff[k] = static_cast<uint32_t>((32 * k + lane) * 16);   // transposed V: d rows
+    } else {
+      koff[k] = page_off(ktok, 2 * k + kch);
+      voff[k] = page_off(vtok, 2 * k + vch);
+    }
   }
+  // FP8: tokens of score rows gid and gid + 8
+  const int srow0 = KV8 ? sigma_row(gid) : gid;
+  const int srow1 = KV8 ? sigma_row(gid + 8) : gid + 8;
   // Smallest visibility limit of this warp's rows: pages wholly below it (and
   // below the context end) need no masking.
   int minlim = 0x7fffffff;
@@ -386,8 +469,8 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       tok0[k] = sidx[k] = 0;
       if (k < nstep) {
         const int pg = it + k * PL;
-        const int s = pg % kStages;
-        const uint32_t ph = static_cast<uint32_t>(pg / kStages) & 1u;
+        const int s = pg % NS;
+        const uint32_t ph = static_cast<uint32_t>(pg / NS) & 1u;
         if (!aborted && !mbar_wait(&full[s], ph, p.timeout_ns)) aborted = true;
         okp[k] = !aborted && stage_ok[s];
         sidx[k] = s;
@@ -408,6 +491,33 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 #pragma unroll
     for (int k = 0; k < TP; ++k) {
       if (!okp[k]) continue;
+      if constexpr (KV8) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(r0, r1, r2, r3, kb[k] + koff[c]);
+          const uint32_t a00 = e4m3x2_to_f16x2(r0), a02 = e4m3x2_to_f16x2(r0 >> 16);
+          const uint32_t a01 = e4m3x2_to_f16x2(r1), a03 = e4m3x2_to_f16x2(r1 >> 16);
+          const uint32_t a10 = e4m3x2_to_f16x2(r2), a12 = e4m3x2_to_f16x2(r2 >> 16);
+          const uint32_t a11 = e4m3x2_to_f16x2(r3), a13 = e4m3x2_to_f16x2(r3 >> 16);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            uint32_t b00, b01, b10, b11;
+            if constexpr (kQRegs) {
+              b00 = qf[j][2 * c][0];
+              b01 = qf[j][2 * c][1];
+              b10 = qf[j][2 * c + 1][0];
+              b11 = qf[j][2 * c + 1][1];
+            } else {
+              ldsm_x4(b00, b01, b10, b11,
+                      qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + 2 * c * 32));
+            }
+            mma_f16_16816(sa[k][j], a00, a01, a02, a03, b00, b01);
+            mma_f16_16816(sb[k][j], a10, a11, a12, a13, b10, b11);
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int k2 = 0; k2 < Gm::kKSteps; k2 += 2) {
         uint32_t a[2][4];
@@ -445,8 +555,10 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       mlo[k] = mhi[k] = 0xffffffffu;
       if (nvalid[k] < kBlockSize) {
         const int nv = nvalid[k];
-        mlo[k] = (2 * q4 < nv ? 0x0000ffffu : 0u) | (2 * q4 + 1 < nv ? 0xffff0000u : 0u);
-        mhi[k] = (2 * q4 + 8 < nv ? 0x0000ffffu : 0u) | (2 * q4 + 9 < nv ? 0xffff0000u : 0u);
+        // tokens behind the low / high halves of the first and second A register pairs
+        const int t0 = KV8 ? 4 * q4 : 2 * q4, t2 = KV8 ? 4 * q4 + 2 : 2 * q4 + 8;
+        mlo[k] = (t0 < nv ? 0x0000ffffu : 0u) | (t0 + 1 < nv ? 0xffff0000u : 0u);
+        mhi[k] = (t2 < nv ? 0x0000ffffu : 0u) | (t2 + 1 < nv ? 0xffff0000u : 0u);
       }
     }
 
@@ -464,7 +576,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
         if (!okp[k]) {
           t[k][0] = t[k][1] = t[k][2] = t[k][3] = -CUDART_INF_F;
         } else if (!interior[k]) {
-          const int j0 = tok0[k] + gid, j1 = j0 + 8;
+          const int j0 = tok0[k] + srow0, j1 = tok0[k] + srow1;
           t[k][0] = (j0 <= lim0[j]) ? t[k][0] : -CUDART_INF_F;
           t[k][1] = (j0 <= lim1[j]) ? t[k][1] : -CUDART_INF_F;
           t[k][2] = (j1 <= lim0[j]) ? t[k][2] : -CUDART_INF_F;
@@ -506,6 +618,12 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
         const float p2 = hw_exp2(t[k][2] - mu0), p3 = hw_exp2(t[k][3] - mu1);
         l0[j] += p0 + p2;
         l1[j] += p1 + p3;
+        if constexpr (KV8) {
+          // P^T as one f16 B operand (transposed 8x8 blocks)
+          bh0[k][j] = movmatrix_trans(half2_bits(__floats2half2_rn(p0, p1)));
+          bh1[k][j] = movmatrix_trans(half2_bits(__floats2half2_rn(p2, p3)));
+          continue;
+        }
         // P^T as B operands: bf16 high part and bf16 residual, transposed 8x8 blocks
         const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
         const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
@@ -525,6 +643,37 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     for (int k = 0; k < TP; ++k) {
       if (!okp[k]) continue;
       auto pv = [&](auto tail) {
+        if constexpr (KV8) {
+          // transposed V: rows are head dims; ldmatrix c covers dims 32c .. 32c+31
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(r0, r1, r2, r3, vb[k] + voff[c]);
+            uint32_t a[2][4];
+            a[0][0] = e4m3x2_to_f16x2(r0);
+            a[0][2] = e4m3x2_to_f16x2(r0 >> 16);
+            a[0][1] = e4m3x2_to_f16x2(r1);
+            a[0][3] = e4m3x2_to_f16x2(r1 >> 16);
+            a[1][0] = e4m3x2_to_f16x2(r2);
+            a[1][2] = e4m3x2_to_f16x2(r2 >> 16);
+            a[1][1] = e4m3x2_to_f16x2(r3);
+            a[1][3] = e4m3x2_to_f16x2(r3 >> 16);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if constexpr (decltype(tail)::value) {
+                a[h][0] &= mlo[k];
+                a[h][1] &= mlo[k];
+                a[h][2] &= mhi[k];
+                a[h][3] &= mhi[k];
+              }
+#pragma unroll
+              for (int j = 0; j < NT; ++j)
+                mma_f16_16816(acc[j][2 * c + h], a[h][0], a[h][1], a[h][2], a[h][3],
+                              bh0[k][j], bh1[k][j]);
+            }
+          }
+          return;
+        }
 #pragma unroll
         for (int mt = 0; mt < Gm::kKSteps; ++mt) {
           uint32_t a0, a1, a2, a3;
@@ -611,11 +760,11 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     const int b = GROUP ? members[m] : b_single;
     const size_t orow = (static_cast<size_t>(b) * T + t) * p.Hq + g * G + hl;
     if (direct) {
-      const float inv = 1.f / Ls;
+      const float inv = out_scale / Ls;
       reinterpret_cast<__nv_bfloat162*>(p.out)[(orow * D + d) >> 1] =
           __floats2bfloat162_rn(o0 * inv, o1 * inv);
     } else {
-      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const float inv = Ls > 0.f ? out_scale / Ls : 0.f;
       const size_t pidx = orow * p.max_parts + slot;
       reinterpret_cast<float2*>(p.part_o)[(pidx * D + d) >> 1] = make_float2(o0 * inv, o1 * inv);
       if (d == 0) {
@@ -625,11 +774,11 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   }
 }
 
-template <int D, class C, bool GROUP>
+template <int D, class C, bool GROUP, bool KV8>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                        dim3 grid, cudaStream_t s, bool overlap_previous) {
-  constexpr int smem = Smem<D, C::NT, C::NTW>::kAlloc;
-  auto kern = paged_attn_kernel<D, C, GROUP>;
+  constexpr int smem = Smem<D, C::NT, C::NTW, KV8>::kAlloc;
+  auto kern = paged_attn_kernel<D, C, GROUP, KV8>;
   static int configured_device = -1;         // attribute set once per device in practice
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -659,16 +808,16 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const AttnP
 
 // `rows` = query rows per CTA (1..64).  One n-tile per warp keeps registers low
 // and many warps resident (latency hiding); warp columns split the rows.
-template <int D, bool GROUP>
+template <int D, bool GROUP, bool KV8 = false>
 cudaError_t launch_dispatch(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                             int rows, dim3 grid, cudaStream_t s, bool overlap_previous) {
   const bool o = overlap_previous;
   if (rows <= 0) return cudaErrorInvalidValue;
-  if (rows <= 8) return launch_one<D, Cfg<1, 1, 4, 3>, GROUP>(tk, tv, p, grid, s, o);
-  if (rows <= 16) return launch_one<D, Cfg<1, 2, 2, 3>, GROUP>(tk, tv, p, grid, s, o);
-  if (rows <= 24) return launch_one<D, Cfg<1, 3, 2, 2, 2>, GROUP>(tk, tv, p, grid, s, o);
-  if (rows <= 32) return launch_one<D, Cfg<1, 4, 2, 2>, GROUP>(tk, tv, p, grid, s, o);
-  if (rows <= 64) return launch_one<D, Cfg<2, 4, 1, 2>, GROUP>(tk, tv, p, grid, s, o);
+  if (rows <= 8) return launch_one<D, Cfg<1, 1, 4, 3>, GROUP, KV8>(tk, tv, p, grid, s, o);
+  if (rows <= 16) return launch_one<D, Cfg<1, 2, 2, 3>, GROUP, KV8>(tk, tv, p, grid, s, o);
+  if (rows <= 24) return launch_one<D, Cfg<1, 3, 2, 2, 2>, GROUP, KV8>(tk, tv, p, grid, s, o);
+  if (rows <= 32) return launch_one<D, Cfg<1, 4, 2, 2>, GROUP, KV8>(tk, tv, p, grid, s, o);
+  if (rows <= 64) return launch_one<D, Cfg<2, 4, 1, 2>, GROUP, KV8>(tk, tv, p, grid, s, o);
   return cudaErrorInvalidValue;
 }
 

@@ -32,6 +32,8 @@ struct AttnParams {
                                   //   domain, softmax denominator) per partition
   const int32_t* seq_group;       // [B] or nullptr
   const int32_t* group_prefix_blocks;  // [num_groups] or nullptr
+  const float* k_scale;           // FP8 pages: [Hkv] dequantisation scales of K and V
+  const float* v_scale;           //   (nullptr for bf16 pages)
   int mbs;                        // max_blocks_per_seq
   int max_ctx;                    // bound on context_lens
   int num_seqs, T, Hq, Hkv, G, num_blocks;
@@ -56,6 +58,15 @@ cudaError_t launch_attn_group_d64(const CUtensorMap& tk, const CUtensorMap& tv,
                                   const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_group_d128(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
+// FP8 (E4M3) pages: K [NB, Hkv, 16, D] token-major, V [NB, Hkv, D, 16] per-page transposed.
+cudaError_t launch_attn8_d64(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                             int rows, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn8_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                              int rows, dim3 grid, cudaStream_t s);
+cudaError_t launch_reshape_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slots, const float* k_scale, const float* v_scale,
+                               int num_tokens, int num_blocks, int hkv, int head_dim,
+                               cudaStream_t s);
 cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_blocks, int hkv,
@@ -70,6 +81,8 @@ cudaError_t take_error_attn_d64(unsigned* bits);
 cudaError_t take_error_attn_d128(unsigned* bits);
 cudaError_t take_error_group_d64(unsigned* bits);
 cudaError_t take_error_group_d128(unsigned* bits);
+cudaError_t take_error_attn8_d64(unsigned* bits);
+cudaError_t take_error_attn8_d128(unsigned* bits);
 cudaError_t take_error_misc(unsigned* bits);
 
 }  // namespace pa

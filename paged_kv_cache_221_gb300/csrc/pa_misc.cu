@@ -48,6 +48,72 @@ cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, vo
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- reshape_and_cache (FP8)
+// One thread per 8 head dims of one (token, kv head): each bf16 value x is
+// stored as the E4M3 code nearest to x / scale[head] (IEEE float32 division,
+// round to nearest even, saturating to +-448).  K pages are token-major
+// [NB, Hkv, 16, D]; V pages are transposed [NB, Hkv, D, 16].
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                 uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                                 const int64_t* __restrict__ slots,
+                                 const float* __restrict__ k_scale,
+                                 const float* __restrict__ v_scale, int num_tokens, int hkv,
+                                 int head_dim, long long num_slots) {
+  const int vecs = head_dim / 8;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(num_tokens) * hkv * vecs;
+  if (idx >= total) return;
+  const int v = static_cast<int>(idx % vecs);
+  const long long th = idx / vecs;
+  const int h = static_cast<int>(th % hkv);
+  const long long i = th / hkv;
+  const long long s = slots[i];
+  if (s < 0) return;                        // padding token
+  if (s >= num_slots) {
+    atomicOr(&g_pa_err, kErrBounds);
+    return;
+  }
+  const long long blk = s / kBlockSize, off = s % kBlockSize;
+  const size_t src = (static_cast<size_t>(i) * hkv + h) * vecs + v;
+  const uint4 kx = key[src], vx = value[src];
+  const float ks = k_scale[h], vs = v_scale[h];
+  const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
+  const uint32_t vw[4] = {vx.x, vx.y, vx.z, vx.w};
+  uint32_t kc[2] = {0u, 0u};
+  const size_t page = static_cast<size_t>(blk) * hkv + h;
+  uint8_t* vdst = v_cache + (page * head_dim + 8 * v) * kBlockSize + off;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t kp = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(kw[e]), ks),
+                                        __fdiv_rn(bf16_hi(kw[e]), ks));
+    const uint32_t vp = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(vw[e]), vs),
+                                        __fdiv_rn(bf16_hi(vw[e]), vs));
+    kc[e >> 1] |= kp << (16 * (e & 1));
+    vdst[(2 * e) * kBlockSize] = static_cast<uint8_t>(vp & 0xFFu);
+    vdst[(2 * e + 1) * kBlockSize] = static_cast<uint8_t>(vp >> 8);
+  }
+  *reinterpret_cast<uint2*>(k_cache + (page * kBlockSize + off) * head_dim + 8 * v) =
+      make_uint2(kc[0], kc[1]);
+}
+
+cudaError_t launch_reshape_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slots, const float* k_scale, const float* v_scale,
+                               int num_tokens, int num_blocks, int hkv, int head_dim,
+                               cudaStream_t s) {
+  const long long total = static_cast<long long>(num_tokens) * hkv * (head_dim / 8);
+  if (total == 0) return cudaSuccess;
+  const long long blocks = (total + 255) / 256;
+  reshape_and_cache_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), slots, k_scale, v_scale,
+      num_tokens, hkv, head_dim, static_cast<long long>(num_blocks) * kBlockSize);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- copy_blocks
 // Copy-on-write support: whole physical blocks (every kv head, K and V) are
 // copied from pairs[i][0] to pairs[i][1], bits unchanged.  Grid: (chunks of

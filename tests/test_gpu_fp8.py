@@ -1,0 +1,236 @@
+"""Parity of the FP8 (E4M3) page path (through the C ABI) with the fp64 FP8 oracle.
+
+reshape_and_cache_fp8 is compared code for code over the whole pool.  Attention
+outputs (bf16) must be within max abs error 1e-2 and relative L2 error 2e-3 of
+attention over the dequantised pages in fp64.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import fp8 as F
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():          # collected on CPU-only hosts, never run there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import __graft_entry__  # noqa: E402
+
+__graft_entry__.build()
+
+import paged_kv_cache_221_gb300 as pa  # noqa: E402
+from gpu_util import assert_close, to_dev  # noqa: E402
+
+
+@pytest.fixture(autouse=True)
+def no_device_error():
+    yield
+    assert pa.get_device_error() == 0, "device error word was set"
+
+
+class Dev8:
+    """Device copies of an FP8 workload."""
+
+    def __init__(self, w):
+        self.w = w
+        self.q = to_dev(w.q)
+        self.k = to_dev(w.k_codes)
+        self.v = to_dev(w.v_codes)
+        self.ks = to_dev(w.k_scale)
+        self.vs = to_dev(w.v_scale)
+        self.tables = to_dev(w.block_tables)
+        self.lens = to_dev(w.context_lens)
+        self.new_key = to_dev(w.new_key)
+        self.new_value = to_dev(w.new_value)
+        self.slots = to_dev(w.slot_mapping)
+
+    def reshape(self):
+        pa.reshape_and_cache_fp8(self.new_key, self.new_value, self.k, self.v, self.slots,
+                                 self.ks, self.vs)
+
+    def attend(self, partition_size=None, workspace=None, out=None):
+        w = self.w
+        ps = w.partition_size if partition_size is None else partition_size
+        return pa.verify_fp8(self.q, self.k, self.v, self.ks, self.vs, self.tables, self.lens,
+                             w.max_context_len, w.scale, ps, workspace, out)
+
+
+def codes(t):
+    return t.detach().cpu().numpy()
+
+
+def fp8(name, size="small"):
+    base = (W.SMALL if size == "small" else W.FULL)[name]()
+    base.seq_group = None                    # FP8 pages: the per-sequence path
+    base.group_prefix_blocks = None
+    return W.fp8_variant(base, seed=len(name))
+
+
+NAMES = ["tiny", "decode_8b", "decode_70b", "spec_verify", "shared_prefix"]
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_small_config_matches_oracle(name):
+    w = fp8(name)
+    ref, kref, vref = F.run_workload(w)
+    d = Dev8(w)
+    d.reshape()
+    np.testing.assert_array_equal(codes(d.k), kref)
+    np.testing.assert_array_equal(codes(d.v), vref)
+    assert_close(d.attend(), ref, what=f"{name} fp8")
+
+
+@pytest.mark.parametrize("name", ["decode_8b", "spec_verify", "decode_70b"])
+@pytest.mark.parametrize("psize", [16, 48, 512, 0])
+def test_partition_sizes(name, psize):
+    w = fp8(name)
+    ref, _, _ = F.run_workload(w)
+    d = Dev8(w)
+    d.reshape()
+    assert_close(d.attend(partition_size=psize), ref, what=f"{name} fp8 psize {psize}")
+
+
+EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 511, 512, 513]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("hq,hkv,T", [(4, 4, 1), (32, 8, 1), (64, 8, 1), (32, 8, 5), (16, 1, 4),
+                                      (8, 2, 3)])
+def test_edge_lengths_and_head_layouts(D, hq, hkv, T):
+    lens = [max(L, T) for L in EDGE_LENS]
+    base = W.build("edge8", lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=D,
+                   num_query_tokens=T, seed=D + hq + T)
+    w = W.fp8_variant(base, seed=D + T)
+    ref, kref, vref = F.run_workload(w)
+    d = Dev8(w)
+    d.reshape()
+    np.testing.assert_array_equal(codes(d.k), kref)
+    np.testing.assert_array_equal(codes(d.v), vref)
+    for ps in (16, 64, 0):
+        assert_close(d.attend(partition_size=ps), ref, what=f"fp8 D{D} {hq}/{hkv} T{T} ps{ps}")
+
+
+def test_every_code_in_the_pages():
+    """Pages cycling through all 254 finite codes (subnormals, zeros, +-448) with
+    power-of-two scales; K and V use different orders of the codes."""
+    base = W.build("allcodes", [300, 64, 17], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                   seed=9)
+    w = W.fp8_variant(base, seed=9)
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    live = w.k_codes != W.NAN_E4M3
+    w.k_codes[live] = np.resize(finite, int(live.sum()))
+    live = w.v_codes != W.NAN_E4M3
+    w.v_codes[live] = np.resize(finite[::-1], int(live.sum()))
+    w.k_scale = np.array([2.0 ** -7, 2.0 ** -8], dtype=np.float32)
+    w.v_scale = np.array([2.0 ** -6, 2.0 ** -9], dtype=np.float32)
+    ref, _, _ = F.run_workload(w)
+    d = Dev8(w)
+    d.reshape()
+    for ps in (32, 0):
+        assert_close(d.attend(partition_size=ps), ref, what=f"all codes ps{ps}")
+
+
+def test_quantisation_edge_values_bit_exact():
+    """New values at ties, subnormals, saturation and signed zeros, quantised on the GPU
+    exactly as the oracle's float32-divide-then-round rule."""
+    rng = np.random.default_rng(12)
+    N, Hkv, D = 64, 2, 128
+    pos = F.decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (pos[:-1] + pos[1:]) / 2
+    vals = np.concatenate([pos, -pos, mids, -mids, [500.0, -600.0, 1e30, -1e30, 0.0, -0.0,
+                                                    1e-30, -1e-30, 2.0 ** -10, -(2.0 ** -10)]])
+    vals = np.resize(vals, N * Hkv * D).astype(np.float32)
+    rng.shuffle(vals)
+    key = W.f32_to_bf16_bits(vals).reshape(N, Hkv, D)
+    value = W.f32_to_bf16_bits(vals[::-1].copy()).reshape(N, Hkv, D)
+    k_scale = np.array([1.0, 0.5], dtype=np.float32)           # exact ties survive the divide
+    v_scale = np.array([0.25, 0.0137], dtype=np.float32)
+    NB = 8
+    kc = np.full((NB, Hkv, 16, D), 0x7F, dtype=np.uint8)
+    vc = np.full((NB, Hkv, D, 16), 0x7F, dtype=np.uint8)
+    slots = rng.permutation(NB * 16)[:N].astype(np.int64)
+    kref, vref = F.reshape_and_cache(key, value, kc, vc, slots, k_scale, v_scale, 16)
+    dk, dv = to_dev(kc), to_dev(vc)
+    pa.reshape_and_cache_fp8(to_dev(key), to_dev(value), dk, dv, to_dev(slots),
+                             to_dev(k_scale), to_dev(v_scale))
+    np.testing.assert_array_equal(codes(dk), kref)
+    np.testing.assert_array_equal(codes(dv), vref)
+
+
+def test_nan_input_stays_nan():
+    key = np.full((1, 1, 64), 0x7FC0, dtype=np.uint16)           # bf16 NaN
+    value = np.full((1, 1, 64), 0xFFC0, dtype=np.uint16)         # negative NaN
+    kc = np.zeros((2, 1, 16, 64), dtype=np.uint8)
+    vc = np.zeros((2, 1, 64, 16), dtype=np.uint8)
+    dk, dv = to_dev(kc), to_dev(vc)
+    one = to_dev(np.ones(1, dtype=np.float32))
+    pa.reshape_and_cache_fp8(to_dev(key), to_dev(value), dk, dv,
+                             to_dev(np.array([19], dtype=np.int64)), one, one)
+    k, v = codes(dk), codes(dv)
+    assert set(np.unique(k[1, 0, 3, :]).tolist()) <= {0x7F, 0xFF}
+    assert set(np.unique(v[1, 0, :, 3]).tolist()) <= {0x7F, 0xFF}
+    assert not k[0].any() and not v[0].any()
+
+
+def test_constant_v_gives_one():
+    """V codes all 1.0 with scale 1: the output is 1 up to the f16 rounding of P."""
+    w = fp8("decode_8b")
+    w.v_codes[w.v_codes != W.NAN_E4M3] = 0x38                   # 1.0
+    w.v_scale = np.ones_like(w.v_scale)
+    w.new_value = np.full_like(w.new_value, 0x3F80)              # bf16 1.0
+    d = Dev8(w)
+    d.reshape()
+    for ps in (32, 0):
+        out = d.attend(partition_size=ps).float()
+        assert torch.isfinite(out).all()
+        assert float((out - 1).abs().max()) <= 2e-3
+
+
+def test_bad_block_id_reports_bounds():
+    w = fp8("decode_8b")
+    d = Dev8(w)
+    d.reshape()
+    d.tables[1, 2] = w.num_blocks + 7
+    d.attend(partition_size=64)
+    assert pa.get_device_error() == 5
+
+
+def test_argument_errors():
+    w = fp8("tiny")
+    d = Dev8(w)
+    with pytest.raises(ValueError):                         # V pages must be transposed
+        pa.verify_fp8(d.q, d.k, d.k, d.ks, d.vs, d.tables, d.lens)
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.verify_fp8(d.q, d.k, d.v, d.ks, d.vs, d.tables, d.lens, w.max_context_len, w.scale,
+                      24)                                       # not a block multiple
+    assert e.value.status == 1
+
+
+def sample_seqs(w, n=6, seed=0):
+    L = w.context_lens
+    pick = {int(np.argmin(L)), int(np.argmax(L))}
+    rng = np.random.default_rng(seed)
+    while len(pick) < min(n, w.num_seqs):
+        pick.add(int(rng.integers(w.num_seqs)))
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("name", ["decode_8b", "decode_70b", "spec_verify"])
+def test_full_size_sampled(name):
+    """Full-size FP8 workloads with the default partitions; sampled rows vs the oracle."""
+    w = fp8(name, size="full")
+    d = Dev8(w)
+    d.reshape()
+    out = d.attend()
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out.float()).all())
+    seqs = sample_seqs(w)
+    k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
+                               w.k_scale, w.v_scale, 16)
+    ref = F.paged_attention(w.q, k, v, w.k_scale, w.v_scale, w.block_tables, w.context_lens,
+                            w.scale, w.num_kv_heads, 16, seqs=seqs)
+    assert_close(out, ref, seqs=seqs, what=f"{name} fp8 full")
+    s = w.slot_mapping
+    np.testing.assert_array_equal(codes(d.k)[s // 16, :, s % 16, :], k[s // 16, :, s % 16, :])
