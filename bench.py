@@ -31,7 +31,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "paged decode-attention KV-read GB/s vs GB300 HBM peak; seq-steps/sec"
 KERNEL_SOURCES = ["pa_attn.cuh", "pa_ptx.cuh", "pa_internal.h", "attn_d128.cu", "pa_misc.cu",
-                  "group_d128.cu"]
+                  "group_d128.cu", "attn8_d128.cu"]
 WORKLOAD_DESC = {
     "tiny": "2 seqs (ctx 37, 100), 4 q = 4 kv heads, head_dim 64, 16-block pool",
     "decode_8b": "64 seqs, ctx uniform [512, 4096], 32 q / 8 kv heads, head_dim 128",
@@ -473,7 +473,7 @@ def run_gb300(args):
         "kv_bytes_per_step": kv_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None if fp8 else recorded_traffic(w.name),
+                     "traffic": recorded_traffic(w.name),
                      "kernel": "attention call (paged_attn_kernel + splitkv_reduce_kernel)",
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "launch_ms_avg": round(attn_avg, 5),
