@@ -319,14 +319,13 @@ def run_gb300(args):
     # Per-sequence workloads: one fused call (reshape_and_cache inside the attention
     # launch).  Shared-prefix workload: reshape_and_cache, then the shared-prefix call.
     def reshape():
-        if fp8:
-            pa.reshape_and_cache_fp8(nk, nv, k, v, slots, ks, vs)
-        elif grouped:
+        if grouped:
             pa.reshape_and_cache(nk, nv, k, v, slots)
 
     def attend():
         if fp8:
-            pa.verify_fp8(q, k, v, ks, vs, tables, lens, w.max_context_len, w.scale, ps, ws, out)
+            pa.verify_fp8(q, k, v, ks, vs, tables, lens, w.max_context_len, w.scale, ps, ws, out,
+                          nk, nv)
         elif grouped:
             pa.decode_shared_prefix(q, k, v, tables, lens, sg, gp, w.max_group_size,
                                     w.max_prefix_blocks, w.max_context_len, w.scale, ps, ws, out)
@@ -335,8 +334,8 @@ def run_gb300(args):
                       nk, nv)
 
     # our kernels per step: attention (+ split-KV merge) (+ reshape + shared-prefix kernel)
-    launches_per_step = 1 + (1 if need > 0 else 0) + (2 if grouped else 0) + (1 if fp8 else 0)
-    two_graphs = grouped or fp8
+    launches_per_step = 1 + (1 if need > 0 else 0) + (2 if grouped else 0)
+    two_graphs = grouped
 
     stream = torch.cuda.current_stream(dev)
     # warm-up outside capture (sets kernel attributes), then capture one graph per phase
@@ -480,9 +479,8 @@ def run_gb300(args):
                      "launch_ms_median": round(statistics.median(attn_ms), 5)},
         "clocks": clocks,
         "gpu_launches": launches_per_step * steps,
-        "timing": "CUDA graph of the step replayed (shared-prefix and FP8: reshape graph + "
-                  "attention graph); CUDA events on the launching stream around the attention "
-                  "call",
+        "timing": "CUDA graph of the step replayed (shared-prefix: reshape graph + attention "
+                  "graph); CUDA events on the launching stream around the attention call",
     }
     if e2e is not None:
         line["e2e"] = e2e

@@ -219,6 +219,27 @@ pa_status pa_verify_fp8(void* out, const void* q, const void* k_cache, const voi
                         size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_append_fp8 — pa_reshape_and_cache_fp8 fused into pa_verify_fp8
+ * (the FP8 counterpart of pa_decode_append below): the num_query_tokens new
+ * tokens of every sequence, new_key / new_value bf16 [num_seqs *
+ * num_query_tokens, num_kv_heads, head_dim] in sequence-major order, are
+ * quantised exactly as pa_reshape_and_cache_fp8 does and stored at positions
+ * context_lens[b] - T .. context_lens[b] - 1 of each sequence's pages inside the
+ * attention launch, before those pages are read.  The pools are written, so
+ * they are not const.  Other arguments, requirements and errors as
+ * pa_verify_fp8; new_key and new_value must be 16-byte aligned.
+ */
+pa_status pa_decode_append_fp8(void* out, const void* q, const void* new_key,
+                               const void* new_value, void* k_cache, void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len, int num_seqs,
+                               int num_query_tokens, int num_blocks, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, float scale,
+                               int partition_size, void* workspace, size_t workspace_bytes,
+                               pa_stream_t stream);
+
+/*
  * pa_decode_append — reshape_and_cache fused into the attention call: the K
  * and V vectors of every sequence's num_query_tokens (T) query tokens,
  *   new_key, new_value  [num_seqs, T, num_kv_heads, head_dim]  bf16,

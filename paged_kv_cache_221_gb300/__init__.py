@@ -121,8 +121,13 @@ def verify_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                context_lens: torch.Tensor, max_context_len: Optional[int] = None,
                scale: Optional[float] = None, partition_size: int = 0,
                workspace: Optional[torch.Tensor] = None,
-               out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """``verify`` (T >= 1 query tokens per sequence) over FP8 pages."""
+               out: Optional[torch.Tensor] = None, new_key: Optional[torch.Tensor] = None,
+               new_value: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """``verify`` (T >= 1 query tokens per sequence) over FP8 pages.
+
+    With ``new_key`` / ``new_value`` (bf16, [B*T, Hkv, D] or [B, T, Hkv, D]) the query
+    tokens' K/V are quantised and stored at positions L-T .. L-1 inside the same launch.
+    """
     dev, NB, Hkv, BS, D = _fp8_pools(k_cache, v_cache, k_scale, v_scale)
     _need("q", q, torch.bfloat16, 4, dev)
     _need("block_tables", block_tables, torch.int32, 2, dev)
@@ -142,6 +147,18 @@ def verify_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     need = workspace_size(B, Hq, T, mcl, D, BS, partition_size, 0) if B else 0
     ws, wsb = _workspace(dev, workspace, need)
+    if new_key is not None or new_value is not None:
+        for name, t in (("new_key", new_key), ("new_value", new_value)):
+            if t is None or t.numel() != B * T * Hkv * D:
+                raise ValueError(f"{name} must hold [B, T, Hkv, D] values")
+            _need(name, t, torch.bfloat16, t.dim(), dev)
+        st = library().pa_decode_append_fp8(
+            _vp(out), _vp(q), _vp(new_key), _vp(new_value), _vp(k_cache), _vp(v_cache),
+            _vp(k_scale), _vp(v_scale), _vp(block_tables), block_tables.shape[1],
+            _vp(context_lens), mcl, B, T, NB, Hq, Hkv, D, BS, scale, partition_size, _vp(ws),
+            wsb, _stream(dev))
+        _lib.check("pa_decode_append_fp8", st)
+        return out
     st = library().pa_verify_fp8(_vp(out), _vp(q), _vp(k_cache), _vp(v_cache), _vp(k_scale),
                                  _vp(v_scale), _vp(block_tables), block_tables.shape[1],
                                  _vp(context_lens), mcl, B, T, NB, Hq, Hkv, D, BS, scale,
@@ -155,15 +172,19 @@ def decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                context_lens: torch.Tensor, max_context_len: Optional[int] = None,
                scale: Optional[float] = None, partition_size: int = 0,
                workspace: Optional[torch.Tensor] = None,
-               out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Single-token decode over FP8 pages; q is [B, Hq, D] or [B, 1, Hq, D]."""
+               out: Optional[torch.Tensor] = None, new_key: Optional[torch.Tensor] = None,
+               new_value: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Single-token decode over FP8 pages; q is [B, Hq, D] or [B, 1, Hq, D].
+
+    With ``new_key`` / ``new_value`` ([B, Hkv, D] bf16) the new token is quantised and
+    stored at position L-1 of every sequence inside the same launch."""
     squeeze = q.dim() == 3
     q4 = q.unsqueeze(1) if squeeze else q
     if q4.shape[1] != 1:
         raise ValueError("decode_fp8 takes one query token per sequence (use verify_fp8)")
     o4 = None if out is None else (out.unsqueeze(1) if squeeze else out)
     r = verify_fp8(q4, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                   max_context_len, scale, partition_size, workspace, o4)
+                   max_context_len, scale, partition_size, workspace, o4, new_key, new_value)
     return r.squeeze(1) if squeeze else r
 
 

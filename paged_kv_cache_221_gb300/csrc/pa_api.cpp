@@ -163,7 +163,7 @@ pa_status run_attention(const AttnArgs& a) {
   const bool grouped = a.num_groups > 0;
   if (a.kv8) {
     if (!a.k_scale || !a.v_scale) return PA_ERR_INVALID_ARG;
-    if (a.new_k != nullptr || grouped) return PA_ERR_UNSUPPORTED;
+    if (grouped) return PA_ERR_UNSUPPORTED;
   }
   if (grouped) {
     if (!a.seq_group || !a.group_prefix_blocks || a.max_group_size < 1 ||
@@ -421,6 +421,24 @@ pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const voi
                        max_blocks_per_seq, context_lens, max_context_len, num_seqs, 1,
                        num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale,
                        partition_size, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_append_fp8(void* out, const void* q, const void* new_key,
+                               const void* new_value, void* k_cache, void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len, int num_seqs,
+                               int num_query_tokens, int num_blocks, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, float scale,
+                               int partition_size, void* workspace, size_t workspace_bytes,
+                               pa_stream_t stream) {
+  if (num_seqs > 0 && (!new_key || !new_value)) return PA_ERR_INVALID_ARG;
+  AttnArgs a{out, q, new_key, new_value, k_cache, v_cache, block_tables, max_blocks_per_seq,
+             context_lens, max_context_len, num_seqs, num_query_tokens, num_blocks,
+             num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_size, nullptr,
+             nullptr, 0, 0, 0, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), true, k_scale, v_scale};
+  return run_attention(a);
 }
 
 pa_status pa_decode_append(void* out, const void* q, const void* new_key, const void* new_value,

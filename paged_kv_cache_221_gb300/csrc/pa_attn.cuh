@@ -267,9 +267,10 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       const int cnt = min(32, npages - base);
       for (int j0 = 0; j0 < cnt; j0 += GP) {
         const int jn = min(j0 + GP, cnt);
-        if constexpr (!GROUP && !KV8) {
+        if constexpr (!GROUP) {
           // Query tokens' K/V that land in these pages are stored into the pool
-          // first (reshape_and_cache fused), then the pages are read by TMA.
+          // first (reshape_and_cache fused; FP8 pages quantise on the way), then
+          // the pages are read by TMA.
           if (p.new_k != nullptr) {
             bool wrote = false;                 // warp-uniform
             for (int j = j0; j < jn; ++j) {
@@ -278,18 +279,46 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
               const int lo = max(vlen - T, pos0), hi = min(vlen - 1, pos0 + kBlockSize - 1);
               if (lo > hi || static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks))
                 continue;
-              constexpr int CH = D / 8;         // 16-byte chunks per row
               for (int pos = lo; pos <= hi; ++pos) {
                 const size_t src =
                     (static_cast<size_t>(b_single) * T + (pos - (vlen - T))) * p.Hkv + g;
-                const size_t dst = (static_cast<size_t>(phys) * p.Hkv + g) * kBlockSize +
-                                   (pos & (kBlockSize - 1));
-                for (int c = lane; c < 2 * CH; c += 32) {
-                  const bool isv = c >= CH;
-                  const int cc = isv ? c - CH : c;
-                  const uint4 v =
-                      reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + cc];
-                  reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + cc] = v;
+                const size_t page = static_cast<size_t>(phys) * p.Hkv + g;
+                const int off = pos & (kBlockSize - 1);
+                if constexpr (KV8) {
+                  // lane c: head dims 4c .. 4c+3; K row bytes contiguous, V bytes
+                  // one per transposed row
+                  const float ks = p.k_scale[g], vs = p.v_scale[g];
+                  for (int c = lane; c < D / 4; c += 32) {
+                    const uint2 kx = reinterpret_cast<const uint2*>(p.new_k)[src * (D / 4) + c];
+                    const uint2 vx = reinterpret_cast<const uint2*>(p.new_v)[src * (D / 4) + c];
+                    const uint32_t k01 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(kx.x), ks),
+                                                         __fdiv_rn(bf16_hi(kx.x), ks));
+                    const uint32_t k23 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(kx.y), ks),
+                                                         __fdiv_rn(bf16_hi(kx.y), ks));
+                    const uint32_t v01 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(vx.x), vs),
+                                                         __fdiv_rn(bf16_hi(vx.x), vs));
+                    const uint32_t v23 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(vx.y), vs),
+                                                         __fdiv_rn(bf16_hi(vx.y), vs));
+                    uint8_t* kp = static_cast<uint8_t*>(p.k_pool);
+                    uint8_t* vp = static_cast<uint8_t*>(p.v_pool);
+                    *reinterpret_cast<uint32_t*>(kp + (page * kBlockSize + off) * D + 4 * c) =
+                        k01 | (k23 << 16);
+                    uint8_t* vrow = vp + (page * D + 4 * c) * kBlockSize + off;
+                    vrow[0] = static_cast<uint8_t>(v01 & 0xFFu);
+                    vrow[kBlockSize] = static_cast<uint8_t>(v01 >> 8);
+                    vrow[2 * kBlockSize] = static_cast<uint8_t>(v23 & 0xFFu);
+                    vrow[3 * kBlockSize] = static_cast<uint8_t>(v23 >> 8);
+                  }
+                } else {
+                  constexpr int CH = D / 8;     // 16-byte chunks per row
+                  const size_t dst = page * kBlockSize + off;
+                  for (int c = lane; c < 2 * CH; c += 32) {
+                    const bool isv = c >= CH;
+                    const int cc = isv ? c - CH : c;
+                    const uint4 v =
+                        reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + cc];
+                    reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + cc] = v;
+                  }
                 }
               }
               wrote = true;

@@ -53,8 +53,6 @@ cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, vo
 // stored as the E4M3 code nearest to x / scale[head] (IEEE float32 division,
 // round to nearest even, saturating to +-448).  K pages are token-major
 // [NB, Hkv, 16, D]; V pages are transposed [NB, Hkv, D, 16].
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 __global__ void __launch_bounds__(256)
     reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,

@@ -191,6 +191,10 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// The two bf16 halves of a 32-bit word as floats (low half, high half).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
 // bf16x2 -> f16x2 (exact for magnitudes in [2^-14, 65504]).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&v);

@@ -56,6 +56,14 @@ class Dev8:
         return pa.verify_fp8(self.q, self.k, self.v, self.ks, self.vs, self.tables, self.lens,
                              w.max_context_len, w.scale, ps, workspace, out)
 
+    def attend_append(self, partition_size=None):
+        """reshape_and_cache_fp8 fused into the attention launch (pa_decode_append_fp8)."""
+        w = self.w
+        ps = w.partition_size if partition_size is None else partition_size
+        return pa.verify_fp8(self.q, self.k, self.v, self.ks, self.vs, self.tables, self.lens,
+                             w.max_context_len, w.scale, ps, None, None, self.new_key,
+                             self.new_value)
+
 
 def codes(t):
     return t.detach().cpu().numpy()
@@ -208,6 +216,35 @@ def test_argument_errors():
     assert e.value.status == 1
 
 
+@pytest.mark.parametrize("name", ["tiny", "decode_8b", "decode_70b", "spec_verify"])
+@pytest.mark.parametrize("psize", [32, 0])
+def test_append_matches_oracle(name, psize):
+    """The fused append writes the same codes as reshape_and_cache_fp8 and attends correctly."""
+    w = fp8(name)
+    ref, kref, vref = F.run_workload(w)
+    d = Dev8(w)
+    out = d.attend_append(partition_size=psize)
+    np.testing.assert_array_equal(codes(d.k), kref)
+    np.testing.assert_array_equal(codes(d.v), vref)
+    assert_close(out, ref, what=f"{name} fp8 append ps{psize}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_append_edge_lengths(D):
+    lens = [max(L, 3) for L in EDGE_LENS]
+    base = W.build("edge8_append", lens, num_q_heads=16, num_kv_heads=4, head_dim=D,
+                   num_query_tokens=3, seed=78 + D)
+    w = W.fp8_variant(base, seed=5)
+    ref, kref, vref = F.run_workload(w)
+    d = Dev8(w)
+    for ps in (16, 0):
+        d = Dev8(w)
+        out = d.attend_append(partition_size=ps)
+        assert_close(out, ref, what=f"fp8 append edge D{D} ps{ps}")
+    np.testing.assert_array_equal(codes(d.k), kref)
+    np.testing.assert_array_equal(codes(d.v), vref)
+
+
 def sample_seqs(w, n=6, seed=0):
     L = w.context_lens
     pick = {int(np.argmin(L)), int(np.argmax(L))}
@@ -219,11 +256,11 @@ def sample_seqs(w, n=6, seed=0):
 
 @pytest.mark.parametrize("name", ["decode_8b", "decode_70b", "spec_verify"])
 def test_full_size_sampled(name):
-    """Full-size FP8 workloads with the default partitions; sampled rows vs the oracle."""
+    """Full-size FP8 workloads in the benchmark's launch configuration (fused append,
+    default partitions); sampled rows vs the oracle."""
     w = fp8(name, size="full")
     d = Dev8(w)
-    d.reshape()
-    out = d.attend()
+    out = d.attend_append()
     torch.cuda.synchronize()
     assert bool(torch.isfinite(out.float()).all())
     seqs = sample_seqs(w)
