@@ -333,6 +333,46 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pair
                          int block_size, pa_stream_t stream);
 
 /*
+ * pa_spec_accept — speculative decoding, after pa_verify: which of the K draft
+ * tokens of each sequence the target keeps, and the one token the target then
+ * emits ("ranksignal" post, Spéculer : plusieurs tokens par passe: drafts are
+ * kept while they agree with the target, the first disagreement drops every
+ * later draft, and the target adds one token of its own; "LLM inference
+ * optimization: KV cache", §5.2 and §5.3: with rejection sampling the output
+ * follows the target's distribution exactly).
+ *
+ *   target_probs     [num_seqs, K + 1, vocab]  float32  target probabilities at
+ *                    the K draft positions and the bonus position K
+ *   draft_probs      [num_seqs, K, vocab]      float32  (sampling only)
+ *   draft_tokens     [num_seqs, K]             int32
+ *   accept_uniforms  [num_seqs, K]             uint32   low 24 bits used (sampling)
+ *   sample_uniforms  [num_seqs]                uint32   (sampling)
+ *   out_tokens       [num_seqs, K + 1]         int32    kept drafts, then the emitted
+ *                    token, then -1
+ *   num_accepted     [num_seqs]                int32    number of kept drafts
+ *
+ * greedy != 0: draft i is kept while it equals the most probable token of row
+ * i (lowest index on ties); the emitted token is the most probable token of the
+ * first row whose draft differs (row K if every draft is kept).
+ * greedy == 0 (rejection sampling): draft x_i is kept iff
+ * draft_probs[i][x_i] * a_i < target_probs[i][x_i] * 2^24 (a_i = low 24 bits of
+ * accept_uniforms, compared exactly); the emitted token is drawn from
+ * max(0, p_i - q_i) (float32) at the first rejected position i, or from p_K,
+ * by an exact integer inverse-CDF draw: weights w(x) = floor(r(x) * 2^40), W =
+ * sum w, token = the smallest x whose prefix sum of w exceeds
+ * floor(sample_uniform * W / 2^32); if W = 0, the most probable token of that
+ * row.  The result does not depend on summation order.
+ * Requirements: 1 <= vocab <= 2^19, 0 <= K <= 64, probabilities finite and in
+ * [0, 1].  A draft token outside [0, vocab) sets PA_ERR_BOUNDS on the device
+ * and is treated as not kept.  One CTA per sequence; all device pointers.
+ */
+pa_status pa_spec_accept(const float* target_probs, const float* draft_probs,
+                         const int32_t* draft_tokens, const uint32_t* accept_uniforms,
+                         const uint32_t* sample_uniforms, int num_seqs, int num_drafts,
+                         int vocab_size, int greedy, int32_t* out_tokens, int32_t* num_accepted,
+                         pa_stream_t stream);
+
+/*
  * Block manager — host-side bookkeeping of the physical block pool (no device
  * memory, no CUDA calls): sequences own ordered lists of physical blocks (their
  * block tables); forked sequences share blocks through reference counts; the

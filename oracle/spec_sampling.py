@@ -25,8 +25,8 @@ inference optimization: KV cache", §5.3).  Two rules:
 The random numbers are inputs, and every decision is written in exact
 arithmetic so that any correct implementation reaches the same tokens:
 
-* acceptance uses a 24-bit uniform a_i: keep iff q * a_i < p * 2^24, both sides
-  exact in fp64 (p, q are float32);
+* acceptance uses a 24-bit uniform a_i (the low 24 bits of the given integer):
+  keep iff q * a_i < p * 2^24, both sides exact in fp64 (p, q are float32);
 * the final draw uses a 32-bit uniform s and weights quantised to multiples of
   2^-40: w(x) = floor(r(x) * 2^40) with r(x) = max(0, p(x) - q(x)) evaluated in
   float32 (or r = p at the bonus position); W = sum of w; the token is the
@@ -52,7 +52,7 @@ def argmax_lowest(p) -> int:
 
 def keep_draft(p_x, q_x, a24) -> bool:
     """Rejection test: keep iff a24 / 2^24 < p / q, written as q * a24 < p * 2^24 (exact)."""
-    return float(np.float32(q_x)) * float(a24) < float(np.float32(p_x)) * TWO24
+    return float(np.float32(q_x)) * float(int(a24) & 0xFFFFFF) < float(np.float32(p_x)) * TWO24
 
 
 def residual(p_row, q_row) -> np.ndarray:

@@ -363,6 +363,41 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs) -> None:
     _lib.check("pa_copy_blocks", st)
 
 
+def spec_accept(target_probs: torch.Tensor, draft_tokens: torch.Tensor,
+                draft_probs: Optional[torch.Tensor] = None,
+                accept_uniforms: Optional[torch.Tensor] = None,
+                sample_uniforms: Optional[torch.Tensor] = None, greedy: bool = False):
+    """Speculative acceptance after verify: (out_tokens [B, K+1] int32, num_accepted [B]).
+
+    target_probs float32 [B, K+1, V]; draft_tokens int32 [B, K]; for sampling also
+    draft_probs float32 [B, K, V], accept_uniforms uint32-valued int32/int64 [B, K] (low 24
+    bits used) and sample_uniforms [B] (32-bit values).  Uniform tensors are passed as
+    int32 views of the 32-bit patterns.
+    """
+    _need("target_probs", target_probs, torch.float32, 3)
+    dev = target_probs.device
+    B, K1, V = target_probs.shape
+    K = K1 - 1
+    _need("draft_tokens", draft_tokens, torch.int32, 2, dev)
+    if tuple(draft_tokens.shape) != (B, K):
+        raise ValueError("draft_tokens must be [B, K]")
+    if not greedy:
+        _need("draft_probs", draft_probs, torch.float32, 3, dev)
+        _need("accept_uniforms", accept_uniforms, torch.int32, 2, dev)
+        _need("sample_uniforms", sample_uniforms, torch.int32, 1, dev)
+        if tuple(draft_probs.shape) != (B, K, V) or tuple(accept_uniforms.shape) != (B, K) \
+                or sample_uniforms.shape[0] != B:
+            raise ValueError("inconsistent shapes")
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    kept = torch.empty(B, dtype=torch.int32, device=dev)
+    st = library().pa_spec_accept(_vp(target_probs), _vp(draft_probs if not greedy else None),
+                                  _vp(draft_tokens), _vp(accept_uniforms if not greedy else None),
+                                  _vp(sample_uniforms if not greedy else None), B, K, V,
+                                  1 if greedy else 0, _vp(out), _vp(kept), _stream(dev))
+    _lib.check("pa_spec_accept", st)
+    return out, kept
+
+
 class BlockManager:
     """Host-side block manager of the paged KV cache (the library's native C++ manager).
 

@@ -475,6 +475,27 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
   return run_attention(a);
 }
 
+pa_status pa_spec_accept(const float* target_probs, const float* draft_probs,
+                         const int32_t* draft_tokens, const uint32_t* accept_uniforms,
+                         const uint32_t* sample_uniforms, int num_seqs, int num_drafts,
+                         int vocab_size, int greedy, int32_t* out_tokens, int32_t* num_accepted,
+                         pa_stream_t stream) {
+  if (num_seqs < 0 || num_drafts < 0 || vocab_size < 1) return PA_ERR_INVALID_ARG;
+  if (vocab_size > kMaxSpecVocab || num_drafts > 64 || num_seqs > (1 << 30))
+    return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (!target_probs || !out_tokens || !num_accepted || (num_drafts > 0 && !draft_tokens))
+    return PA_ERR_INVALID_ARG;
+  if (!greedy && (!sample_uniforms || (num_drafts > 0 && (!draft_probs || !accept_uniforms))))
+    return PA_ERR_INVALID_ARG;
+  return launch_spec_accept(target_probs, draft_probs, draft_tokens, accept_uniforms,
+                            sample_uniforms, num_seqs, num_drafts, vocab_size, greedy != 0,
+                            out_tokens, num_accepted,
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 pa_status pa_get_device_error(pa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
@@ -482,7 +503,8 @@ pa_status pa_get_device_error(pa_stream_t stream) {
   if (take_error_attn_d64(&bits) != cudaSuccess || take_error_attn_d128(&bits) != cudaSuccess ||
       take_error_group_d64(&bits) != cudaSuccess ||
       take_error_group_d128(&bits) != cudaSuccess || take_error_attn8_d64(&bits) != cudaSuccess ||
-      take_error_attn8_d128(&bits) != cudaSuccess || take_error_misc(&bits) != cudaSuccess)
+      take_error_attn8_d128(&bits) != cudaSuccess || take_error_spec(&bits) != cudaSuccess ||
+      take_error_misc(&bits) != cudaSuccess)
     return PA_ERR_CUDA;
   if (bits & kErrTimeout) return PA_ERR_TIMEOUT;
   if (bits & kErrBounds) return PA_ERR_BOUNDS;

@@ -16,6 +16,7 @@ constexpr int kStages = 8;            // pages in flight per CTA (multiple of ev
 constexpr int kMaxRows = 64;          // query rows per CTA (8 n-tiles of 8)
 constexpr int kMaxPartitions = 4096;  // split-KV partitions per sequence (merge smem bound)
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
+constexpr int kMaxSpecVocab = 1 << 19;  // speculative acceptance: largest vocabulary
 
 // Everything an attention launch needs besides the two tensor maps.
 struct AttnParams {
@@ -67,6 +68,11 @@ cudaError_t launch_reshape_fp8(const void* key, const void* value, void* k_cache
                                const int64_t* slots, const float* k_scale, const float* v_scale,
                                int num_tokens, int num_blocks, int hkv, int head_dim,
                                cudaStream_t s);
+// Speculative acceptance (pa_spec.cu): one CTA per sequence.
+cudaError_t launch_spec_accept(const float* p, const float* q, const int32_t* drafts,
+                               const uint32_t* a24, const uint32_t* s32, int num_seqs, int K,
+                               int V, bool greedy, int32_t* out_tokens, int32_t* out_kept,
+                               cudaStream_t s);
 cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_blocks, int hkv,
@@ -83,6 +89,7 @@ cudaError_t take_error_group_d64(unsigned* bits);
 cudaError_t take_error_group_d128(unsigned* bits);
 cudaError_t take_error_attn8_d64(unsigned* bits);
 cudaError_t take_error_attn8_d128(unsigned* bits);
+cudaError_t take_error_spec(unsigned* bits);
 cudaError_t take_error_misc(unsigned* bits);
 
 }  // namespace pa
