@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="decode_8b")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window (positions each query token sees); 0 = none")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="KV page format (fp8 = E4M3 pages with per-kv-head scales; the "
                          "per-sequence path)")
@@ -191,20 +193,35 @@ def cpu_baseline(workload, seconds):
             "seq_steps_per_s": round(d["seq_steps_per_s"], 3)}
 
 
-def workload_config(w, ps, world):
+def workload_config(w, ps, world, window=0):
     base = w.name[:-4] if w.name.endswith("_fp8") else w.name
     desc = WORKLOAD_DESC.get(base, base)
     if w.kv_dtype == "fp8":
         desc += "; FP8 (E4M3) K/V pages, per-kv-head scales, per-sequence path"
+    if window > 0:
+        desc += f"; sliding window of {window} positions (only the pages under the windows " \
+                f"are read and counted)"
     pool = (w.k_codes.nbytes + w.v_codes.nbytes) if w.kv_dtype == "fp8" else 2 * w.k_cache.nbytes
     return {"workload": w.name, "desc": desc, "kv_dtype": w.kv_dtype,
             "num_seqs": w.num_seqs, "query_tokens": w.num_query_tokens,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": w.block_size, "pool_blocks": w.num_blocks,
-            "partition_size": ps, "global_batch": w.num_seqs * world,
+            "partition_size": ps, "global_batch": w.num_seqs * world, "window": window,
             "l2": "inputs larger than L2: each step reads %.2f GB of a %.2f GB pool (L2 129 MB)"
                   % (w.kv_bytes() / 1e9, pool / 1e9),
             "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
+
+
+def window_kv_bytes(w, window):
+    """Algorithmic bytes with a sliding window: every (block, kv head) page from the
+    block of the first query's first visible position to the context end, once."""
+    used = set()
+    for b in range(w.num_seqs):
+        L = int(w.context_lens[b])
+        first = max(0, L - w.num_query_tokens - window + 1) // w.block_size
+        nblk = -(-L // w.block_size)
+        used.update(int(x) for x in w.block_tables[b, first:nblk])
+    return len(used) * w.num_kv_heads * w.page_bytes()
 
 
 def data_desc(w):
@@ -293,6 +310,9 @@ def run_gb300(args):
         w.seq_group = None                  # FP8 pages run the per-sequence path
         w.group_prefix_blocks = None
         w = W.fp8_variant(w, seed=rank)
+    if args.window > 0:
+        w.seq_group = None                  # the window runs the per-sequence path
+        w.group_prefix_blocks = None
     ps = w.partition_size if args.partition_size < 0 else args.partition_size
 
     def td(a):
@@ -314,7 +334,7 @@ def run_gb300(args):
                              ps, w.max_prefix_blocks if grouped else 0)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
-    kv_bytes = w.kv_bytes()
+    kv_bytes = w.kv_bytes() if args.window <= 0 else window_kv_bytes(w, args.window)
 
     # Per-sequence workloads: one fused call (reshape_and_cache inside the attention
     # launch).  Shared-prefix workload: reshape_and_cache, then the shared-prefix call.
@@ -323,7 +343,10 @@ def run_gb300(args):
             pa.reshape_and_cache(nk, nv, k, v, slots)
 
     def attend():
-        if fp8:
+        if args.window > 0:
+            pa.attention(q, k, v, tables, lens, w.max_context_len, w.scale, ps, ws, out, nk, nv,
+                         window_size=args.window, k_scale=ks, v_scale=vs)
+        elif fp8:
             pa.verify_fp8(q, k, v, ks, vs, tables, lens, w.max_context_len, w.scale, ps, ws, out,
                           nk, nv)
         elif grouped:
@@ -467,7 +490,7 @@ def run_gb300(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 KV / f16 MMA / fp32 softmax" if fp8 else "bf16",
         "data": data_desc(w),
-        "config": workload_config(w, ps, world),
+        "config": workload_config(w, ps, world, args.window),
         "seq_steps_per_s": round(w.num_seqs * world * steps / (ms_total * 1e-3), 1),
         "kv_bytes_per_step": kv_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,

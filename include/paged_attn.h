@@ -218,6 +218,37 @@ pa_status pa_verify_fp8(void* out, const void* q, const void* k_cache, const voi
                         float scale, int partition_size, void* workspace,
                         size_t workspace_bytes, pa_stream_t stream);
 
+/* KV page formats for pa_attention. */
+enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 };
+
+/*
+ * pa_attention — the general per-sequence call; pa_decode, pa_verify,
+ * pa_decode_append and their _fp8 forms are special cases of it.
+ *   kv_dtype     PA_KV_BF16 (pools as in pa_decode) or PA_KV_FP8_E4M3 (pools and
+ *                scales as in pa_decode_fp8; k_scale / v_scale ignored for bf16)
+ *   new_key,
+ *   new_value    NULL, or the query tokens' K/V (bf16 [num_seqs *
+ *                num_query_tokens, num_kv_heads, head_dim]) to store at positions
+ *                context_lens[b] - T .. context_lens[b] - 1 inside the launch, as
+ *                pa_decode_append / pa_decode_append_fp8 do (both or neither)
+ *   window_size  0: every query token sees its whole causal context.  W > 0: a
+ *                sliding window; query token t, at position pos = context_lens[b]
+ *                - T + t, sees only positions j with pos - W < j <= pos, and
+ *                blocks wholly before the first query's window are not read.
+ * Cited for the window: "ranksignal" post, the attention-kernels section
+ * (sliding-window attention looks only at the latest tokens; the window size
+ * is a parameter).  Other arguments, requirements and errors as pa_verify;
+ * window_size < 0 is PA_ERR_INVALID_ARG.
+ */
+pa_status pa_attention(void* out, const void* q, const void* new_key, const void* new_value,
+                       void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,
+                       int kv_dtype, int window_size, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                       int num_seqs, int num_query_tokens, int num_blocks, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, float scale,
+                       int partition_size, void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream);
+
 /*
  * pa_decode_append_fp8 — pa_reshape_and_cache_fp8 fused into pa_verify_fp8
  * (the FP8 counterpart of pa_decode_append below): the num_query_tokens new

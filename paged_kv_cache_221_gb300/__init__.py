@@ -167,6 +167,56 @@ def verify_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     return out
 
 
+def attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              block_tables: torch.Tensor, context_lens: torch.Tensor,
+              max_context_len: Optional[int] = None, scale: Optional[float] = None,
+              partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+              out: Optional[torch.Tensor] = None, new_key: Optional[torch.Tensor] = None,
+              new_value: Optional[torch.Tensor] = None, window_size: int = 0,
+              k_scale: Optional[torch.Tensor] = None,
+              v_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The general per-sequence call (``pa_attention``): q [B, T, Hq, D]; bf16 pools, or FP8
+    pools when ``k_scale`` / ``v_scale`` are given; optional fused append of the query
+    tokens' K/V; ``window_size`` > 0 for sliding-window attention (each query token sees
+    its last ``window_size`` positions)."""
+    fp8 = k_scale is not None
+    if fp8:
+        dev, NB, Hkv, BS, D = _fp8_pools(k_cache, v_cache, k_scale, v_scale)
+        _need("q", q, torch.bfloat16, 4, dev)
+        _need("block_tables", block_tables, torch.int32, 2, dev)
+        _need("context_lens", context_lens, torch.int32, 1, dev)
+        B, T, Hq, Dq = q.shape
+        if Dq != D or block_tables.shape[0] != B or context_lens.shape[0] != B:
+            raise ValueError("inconsistent shapes")
+        if max_context_len is None:
+            max_context_len = int(context_lens.max().item()) if B else T   # host sync
+        mcl = int(max_context_len)
+        if out is None:
+            out = torch.empty_like(q)
+        else:
+            _need("out", out, torch.bfloat16, 4, dev)
+    else:
+        dev, B, T, Hq, D, NB, Hkv, BS, mcl, out = _attn_common(q, k_cache, v_cache, block_tables,
+                                                              context_lens, max_context_len, out)
+    if (new_key is None) != (new_value is None):
+        raise ValueError("new_key and new_value go together")
+    if new_key is not None:
+        for name, t in (("new_key", new_key), ("new_value", new_value)):
+            if t.numel() != B * T * Hkv * D:
+                raise ValueError(f"{name} must hold [B, T, Hkv, D] values")
+            _need(name, t, torch.bfloat16, t.dim(), dev)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    need = workspace_size(B, Hq, T, mcl, D, BS, partition_size, 0) if B else 0
+    ws, wsb = _workspace(dev, workspace, need)
+    st = library().pa_attention(_vp(out), _vp(q), _vp(new_key), _vp(new_value), _vp(k_cache),
+                                _vp(v_cache), _vp(k_scale), _vp(v_scale), 1 if fp8 else 0,
+                                int(window_size), _vp(block_tables), block_tables.shape[1],
+                                _vp(context_lens), mcl, B, T, NB, Hq, Hkv, D, BS, scale,
+                                partition_size, _vp(ws), wsb, _stream(dev))
+    _lib.check("pa_attention", st)
+    return out
+
+
 def decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
                context_lens: torch.Tensor, max_context_len: Optional[int] = None,

@@ -43,6 +43,8 @@ SIGNATURES = {
                            _i, _f, _i, _vp, _sz, _vp]),
     "pa_verify_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                            _i, _i, _f, _i, _vp, _sz, _vp]),
+    "pa_attention": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i,
+                          _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "pa_decode_append_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i,
                                   _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "pa_bm_create": (_i, [_i, _i, ctypes.POINTER(_vp)]),

@@ -136,6 +136,7 @@ struct AttnArgs {
   bool kv8 = false;                 // FP8 (E4M3) pages with per-kv-head scales
   const float* k_scale = nullptr;
   const float* v_scale = nullptr;
+  int window = 0;                   // sliding window (positions per query), 0 = none
 };
 
 pa_status run_attention(const AttnArgs& a) {
@@ -165,6 +166,8 @@ pa_status run_attention(const AttnArgs& a) {
     if (!a.k_scale || !a.v_scale) return PA_ERR_INVALID_ARG;
     if (grouped) return PA_ERR_UNSUPPORTED;
   }
+  if (a.window < 0) return PA_ERR_INVALID_ARG;
+  if (a.window > 0 && grouped) return PA_ERR_UNSUPPORTED;
   if (grouped) {
     if (!a.seq_group || !a.group_prefix_blocks || a.max_group_size < 1 ||
         a.max_prefix_blocks < 0 ||
@@ -233,6 +236,9 @@ pa_status run_attention(const AttnArgs& a) {
   p.max_parts = plan.max_parts;
   p.max_prefix_blocks = max_prefix;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.window = a.window;
+  p.wcap = a.window > 0 ? static_cast<unsigned>(a.window) : 0x80000000u;
+  p.wspan = a.window > 0 ? a.window : (1 << 30);
   p.timeout_ns = kDefaultTimeoutNs;
 
   const int max_blocks = ceil_div(a.max_context_len, kBlockSize);
@@ -252,8 +258,13 @@ pa_status run_attention(const AttnArgs& a) {
   }
   {
     const int rows = G * a.T;
+    // blocks one sequence may read: all of them, or those under its queries' windows
+    int span = max_blocks;
+    if (a.window > 0)
+      span = static_cast<int>(std::min<long long>(
+          max_blocks, (static_cast<long long>(a.window) + a.T - 1 + kBlockSize - 1) / kBlockSize + 1));
     // 1-D, partition-major: unit u = (partition * num_seqs + seq) * hkv + head
-    const long long units = static_cast<long long>(ceil_div(max_blocks, plan.ppb)) * a.hkv *
+    const long long units = static_cast<long long>(ceil_div(span, plan.ppb)) * a.hkv *
                             a.num_seqs;
     if (units >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(units), 1, 1);
@@ -421,6 +432,25 @@ pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const voi
                        max_blocks_per_seq, context_lens, max_context_len, num_seqs, 1,
                        num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale,
                        partition_size, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_attention(void* out, const void* q, const void* new_key, const void* new_value,
+                       void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,
+                       int kv_dtype, int window_size, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                       int num_seqs, int num_query_tokens, int num_blocks, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, float scale,
+                       int partition_size, void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream) {
+  if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if ((new_key == nullptr) != (new_value == nullptr)) return PA_ERR_INVALID_ARG;
+  AttnArgs a{out, q, new_key, new_value, k_cache, v_cache, block_tables, max_blocks_per_seq,
+             context_lens, max_context_len, num_seqs, num_query_tokens, num_blocks,
+             num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_size, nullptr,
+             nullptr, 0, 0, 0, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), kv_dtype == PA_KV_FP8_E4M3, k_scale,
+             v_scale, window_size};
+  return run_attention(a);
 }
 
 pa_status pa_decode_append_fp8(void* out, const void* q, const void* new_key,

@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <climits>
 #include <type_traits>
 
 #include "pa_ptx.cuh"
@@ -174,11 +175,13 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       return;
     }
     const int nblk = (L + kBlockSize - 1) / kBlockSize;
-    pg0 = pre + unit_p * p.ppb;
+    // With a sliding window, blocks wholly before the first query's window are skipped.
+    const int first = p.window > 0 ? max(pre, max(0, L - T - p.window + 1) / kBlockSize) : pre;
+    pg0 = first + unit_p * p.ppb;
     if (pg0 >= nblk) return;                 // partition past this sequence's end
     pg1 = min(pg0 + p.ppb, nblk);
     const int npre = (pre + p.ppb - 1) / p.ppb;
-    const int nparts = npre + (nblk - pre + p.ppb - 1) / p.ppb;
+    const int nparts = npre + (nblk - first + p.ppb - 1) / p.ppb;
     slot = npre + unit_p;
     direct = (pre == 0 && nparts == 1);
     nrows = G * T;
@@ -427,6 +430,10 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     lim0[j] = lim[rbase + 8 * j + 2 * q4];
     lim1[j] = lim[rbase + 8 * j + 2 * q4 + 1];
   }
+  // Position j is visible to a row with last position lim iff 0 <= lim - j < p.wcap:
+  // wcap is the window, or 2^31 (every earlier position) without one.  Padding
+  // rows (lim = INT_MAX) then see everything without a window and nothing with
+  // one; their columns are never written either way.
   // Q^T B operands: held in registers for NT <= 2, re-read from smem per page otherwise.
   constexpr bool kQRegs = NT <= 2;
   const uint32_t qrow = smem_u32(qs) +
@@ -477,6 +484,8 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   const int srow1 = KV8 ? sigma_row(gid + 8) : gid + 8;
   // Smallest visibility limit of this warp's rows: pages wholly below it (and
   // below the context end) need no masking.
+  // With a window, pages must also start at or after vlen - window, the first
+  // position the sequence's last query token sees (no row's window starts later).
   int minlim = 0x7fffffff;
 #pragma unroll
   for (int j = 0; j < NT; ++j) minlim = min(minlim, min(lim0[j], lim1[j]));
@@ -580,7 +589,8 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 #pragma unroll
     for (int k = 0; k < TP; ++k) {
       nvalid[k] = vlen - tok0[k];
-      interior[k] = okp[k] && (tok0[k] + kBlockSize - 1 <= minlim) && (nvalid[k] >= kBlockSize);
+      interior[k] = okp[k] && (tok0[k] + kBlockSize - 1 <= minlim) &&
+                    (tok0[k] + p.wspan >= vlen) && (nvalid[k] >= kBlockSize);
       mlo[k] = mhi[k] = 0xffffffffu;
       if (nvalid[k] < kBlockSize) {
         const int nv = nvalid[k];
@@ -606,10 +616,11 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
           t[k][0] = t[k][1] = t[k][2] = t[k][3] = -CUDART_INF_F;
         } else if (!interior[k]) {
           const int j0 = tok0[k] + srow0, j1 = tok0[k] + srow1;
-          t[k][0] = (j0 <= lim0[j]) ? t[k][0] : -CUDART_INF_F;
-          t[k][1] = (j0 <= lim1[j]) ? t[k][1] : -CUDART_INF_F;
-          t[k][2] = (j1 <= lim0[j]) ? t[k][2] : -CUDART_INF_F;
-          t[k][3] = (j1 <= lim1[j]) ? t[k][3] : -CUDART_INF_F;
+          const unsigned u0 = static_cast<unsigned>(j0), u1 = static_cast<unsigned>(j1);
+          t[k][0] = (static_cast<unsigned>(lim0[j]) - u0 < p.wcap) ? t[k][0] : -CUDART_INF_F;
+          t[k][1] = (static_cast<unsigned>(lim1[j]) - u0 < p.wcap) ? t[k][1] : -CUDART_INF_F;
+          t[k][2] = (static_cast<unsigned>(lim0[j]) - u1 < p.wcap) ? t[k][2] : -CUDART_INF_F;
+          t[k][3] = (static_cast<unsigned>(lim1[j]) - u1 < p.wcap) ? t[k][3] : -CUDART_INF_F;
         }
         mx0 = fmaxf(mx0, fmaxf(t[k][0], t[k][2]));
         mx1 = fmaxf(mx1, fmaxf(t[k][1], t[k][3]));

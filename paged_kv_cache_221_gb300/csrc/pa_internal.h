@@ -44,6 +44,10 @@ struct AttnParams {
   int num_chunks;                 // shared-prefix kernel: CTAs per group (per partition, head)
   int max_prefix_blocks;          // bound on group_prefix_blocks (launch sizing)
   float scale_log2;               // softmax scale * log2(e)
+  int window;                     // sliding window (positions each query sees), 0 = none
+  unsigned wcap;                  // window, or 2^31 without one (visibility: lim - j < wcap)
+  int wspan;                      // window, or 2^30 without one (interior pages: tok0 +
+                                  //   wspan >= context length)
   unsigned long long timeout_ns;  // limit of every pipeline wait
 };
 

@@ -181,8 +181,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
                       ? p.group_prefix_blocks[p.seq_group[b]] : 0;
   if (pre < 0 || pre > p.max_prefix_blocks || pre * kBlockSize > L) return;
   const int nblk = (L + kBlockSize - 1) / kBlockSize;
+  const int first =
+      p.window > 0 ? max(pre, max(0, L - p.T - p.window + 1) / kBlockSize) : pre;
   const int npre = (pre + p.ppb - 1) / p.ppb;
-  const int nparts = npre + (nblk - pre + p.ppb - 1) / p.ppb;
+  const int nparts = npre + (nblk - first + p.ppb - 1) / p.ppb;
   if (pre == 0 && nparts == 1) return;       // uniform over the CTA
   const bool live = r < rows;
   // row r = t * G + hl  ->  orow = (b*T + t)*Hq + g*G + hl
