@@ -404,6 +404,63 @@ pa_status pa_spec_accept(const float* target_probs, const float* draft_probs,
                          pa_stream_t stream);
 
 /*
+ * Graph runner — CUDA graphs of the attention step for fixed batch-size
+ * classes ("CUDA Graphs, modèles de raisonnement et service désagrégé", §1:
+ * a captured graph replays a whole step with one launch call but needs static
+ * addresses and shapes, so incoming batches are padded to fixed class sizes
+ * such as 1, 2, 4, 8, 16 and the inputs are updated in place before replay).
+ *
+ * pa_runner_create captures, for every class c, one pa_attention call with
+ * num_seqs = c over the caller's static buffers (sized for the largest class;
+ * the runner keeps their addresses, the caller keeps them alive and writes the
+ * step's inputs into them: q, new_key / new_value, block_tables, context_lens
+ * rows 0 .. B-1).  pa_runner_step(B) pads rows B .. c-1 of the smallest class
+ * c >= B with a one-block dummy sequence (context num_query_tokens, every table
+ * entry pad_block, a physical block no sequence uses and that the padded rows'
+ * appends may overwrite), then replays graph c on `stream`.  Output rows 0 .. B-1
+ * are those of pa_attention with num_seqs = B and the same partition_size.
+ * partition_size must be explicit (> 0) so every class splits alike;
+ * max_context_len is the bound every captured launch is sized for.  The
+ * workspace must hold pa_workspace_size(largest class, ...).  The runner owns
+ * one CUDA stream (for capture) and the instantiated graphs, nothing else.
+ * pa_runner_step returns PA_ERR_UNSUPPORTED when B exceeds the largest class.
+ */
+typedef struct pa_runner_config {
+  int num_q_heads, num_kv_heads, head_dim, block_size;
+  int num_query_tokens;
+  int max_blocks_per_seq, max_context_len, num_blocks;
+  int kv_dtype, window_size, partition_size;
+  float scale;
+  int pad_block;
+  int num_classes;
+  const int* classes;          /* host array, strictly increasing, each >= 1 */
+} pa_runner_config;
+
+typedef struct pa_runner_buffers {   /* device pointers, as for pa_attention */
+  void* out;
+  void* q;
+  void* new_key;                     /* NULL: no fused append */
+  void* new_value;
+  int32_t* block_tables;
+  int32_t* context_lens;
+  void* k_cache;
+  void* v_cache;
+  const float* k_scale;              /* FP8 pages only */
+  const float* v_scale;
+  void* workspace;
+  size_t workspace_bytes;
+} pa_runner_buffers;
+
+typedef struct pa_graph_runner pa_graph_runner;
+
+pa_status pa_runner_create(const pa_runner_config* config, const pa_runner_buffers* buffers,
+                           pa_graph_runner** out);
+pa_status pa_runner_step(pa_graph_runner* runner, int num_seqs, pa_stream_t stream);
+/* The class a batch of num_seqs would use, or -1 if none is large enough. */
+int pa_runner_class_of(const pa_graph_runner* runner, int num_seqs);
+void pa_runner_destroy(pa_graph_runner* runner);
+
+/*
  * Block manager — host-side bookkeeping of the physical block pool (no device
  * memory, no CUDA calls): sequences own ordered lists of physical blocks (their
  * block tables); forked sequences share blocks through reference counts; the

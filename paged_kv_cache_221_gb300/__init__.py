@@ -448,6 +448,86 @@ def spec_accept(target_probs: torch.Tensor, draft_tokens: torch.Tensor,
     return out, kept
 
 
+class GraphRunner:
+    """CUDA graphs of the attention step for fixed batch-size classes (``pa_runner_*``).
+
+    The runner captures one ``pa_attention`` call per class over static buffers sized for
+    the largest class, which this object allocates and exposes: write a step's inputs into
+    rows 0 .. B-1 of ``q``, ``new_key``, ``new_value``, ``block_tables`` and
+    ``context_lens``, call ``step(B)``, read rows 0 .. B-1 of ``out``.  Rows B .. c-1 of
+    the class c are padded on the device with a one-block sequence in ``pad_block`` (a
+    physical block no sequence uses).  ``partition_size`` must be explicit.
+    """
+
+    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_q_heads: int,
+                 max_context_len: int, max_blocks_per_seq: int, pad_block: int,
+                 partition_size: int, classes=(1, 2, 4, 8, 16), num_query_tokens: int = 1,
+                 scale: Optional[float] = None, window_size: int = 0, fused_append: bool = True,
+                 k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
+        self._lib = library()
+        fp8 = k_scale is not None
+        if fp8:
+            dev, NB, Hkv, BS, D = _fp8_pools(k_cache, v_cache, k_scale, v_scale)
+        else:
+            _need("k_cache", k_cache, torch.bfloat16, 4)
+            dev = k_cache.device
+            _need("v_cache", v_cache, torch.bfloat16, 4, dev)
+            NB, Hkv, BS, D = k_cache.shape
+        classes = sorted(int(c) for c in classes)
+        Bmax, T = classes[-1], int(num_query_tokens)
+        self.classes = classes
+        self.q = torch.zeros((Bmax, T, num_q_heads, D), dtype=torch.bfloat16, device=dev)
+        self.out = torch.zeros_like(self.q)
+        self.new_key = torch.zeros((Bmax * T, Hkv, D), dtype=torch.bfloat16, device=dev) \
+            if fused_append else None
+        self.new_value = torch.zeros_like(self.new_key) if fused_append else None
+        self.block_tables = torch.full((Bmax, max_blocks_per_seq), pad_block, dtype=torch.int32,
+                                       device=dev)
+        self.context_lens = torch.full((Bmax,), T, dtype=torch.int32, device=dev)
+        need = workspace_size(Bmax, num_q_heads, T, max_context_len, D, BS, partition_size, 0)
+        self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self._keep = (k_cache, v_cache, k_scale, v_scale)
+        self._classes_c = (ctypes.c_int * len(classes))(*classes)
+        cfg = _lib.RunnerConfig(num_q_heads, Hkv, D, BS, T, max_blocks_per_seq, max_context_len,
+                                NB, 1 if fp8 else 0, int(window_size), int(partition_size),
+                                1.0 / math.sqrt(D) if scale is None else float(scale),
+                                int(pad_block), len(classes), self._classes_c)
+        bufs = _lib.RunnerBuffers(self.out.data_ptr(), self.q.data_ptr(),
+                                  self.new_key.data_ptr() if fused_append else None,
+                                  self.new_value.data_ptr() if fused_append else None,
+                                  self.block_tables.data_ptr(), self.context_lens.data_ptr(),
+                                  k_cache.data_ptr(), v_cache.data_ptr(),
+                                  k_scale.data_ptr() if fp8 else None,
+                                  v_scale.data_ptr() if fp8 else None,
+                                  self.workspace.data_ptr(),
+                                  self.workspace.numel())
+        h = ctypes.c_void_p()
+        torch.cuda.synchronize(dev)
+        _lib.check("pa_runner_create", self._lib.pa_runner_create(ctypes.byref(cfg),
+                                                                  ctypes.byref(bufs),
+                                                                  ctypes.byref(h)))
+        self._h = h
+        self.device = dev
+
+    def class_of(self, num_seqs: int) -> int:
+        return int(self._lib.pa_runner_class_of(self._h, num_seqs))
+
+    def step(self, num_seqs: int) -> None:
+        _lib.check("pa_runner_step", self._lib.pa_runner_step(self._h, num_seqs,
+                                                              _stream(self.device)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pa_runner_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class BlockManager:
     """Host-side block manager of the paged KV cache (the library's native C++ manager).
 

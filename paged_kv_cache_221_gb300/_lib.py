@@ -17,6 +17,26 @@ STATUS_NAMES = {
     4: "PA_ERR_CUDA", 5: "PA_ERR_BOUNDS", 6: "PA_ERR_TIMEOUT", 7: "PA_ERR_OUT_OF_BLOCKS",
 }
 
+class RunnerConfig(ctypes.Structure):
+    """pa_runner_config."""
+    _fields_ = [("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("num_query_tokens", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
+                ("max_context_len", ctypes.c_int), ("num_blocks", ctypes.c_int),
+                ("kv_dtype", ctypes.c_int), ("window_size", ctypes.c_int),
+                ("partition_size", ctypes.c_int), ("scale", ctypes.c_float),
+                ("pad_block", ctypes.c_int), ("num_classes", ctypes.c_int),
+                ("classes", ctypes.POINTER(ctypes.c_int))]
+
+
+class RunnerBuffers(ctypes.Structure):
+    """pa_runner_buffers."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("out", "q", "new_key", "new_value",
+                                                 "block_tables", "context_lens", "k_cache",
+                                                 "v_cache", "k_scale", "v_scale", "workspace")] + \
+               [("workspace_bytes", ctypes.c_size_t)]
+
+
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
@@ -58,6 +78,11 @@ SIGNATURES = {
     "pa_bm_num_free_blocks": (_i, [_vp]),
     "pa_bm_ref_count": (_i, [_vp, _i]),
     "pa_bm_num_tokens": (_i, [_vp, _i]),
+    "pa_runner_create": (_i, [ctypes.POINTER(RunnerConfig), ctypes.POINTER(RunnerBuffers),
+                              ctypes.POINTER(_vp)]),
+    "pa_runner_step": (_i, [_vp, _i, _vp]),
+    "pa_runner_class_of": (_i, [_vp, _i]),
+    "pa_runner_destroy": (None, [_vp]),
     "pa_get_device_error": (_i, [_vp]),
     "pa_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
 }

@@ -77,6 +77,10 @@ cudaError_t launch_spec_accept(const float* p, const float* q, const int32_t* dr
                                const uint32_t* a24, const uint32_t* s32, int num_seqs, int K,
                                int V, bool greedy, int32_t* out_tokens, int32_t* out_kept,
                                cudaStream_t s);
+// Graph runner padding: rows [from, to) become a one-block sequence of `len` tokens
+// in block `pad_block`.
+cudaError_t launch_pad_rows(int32_t* block_tables, int32_t* context_lens, int from, int to,
+                            int max_blocks_per_seq, int pad_block, int len, cudaStream_t s);
 cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_blocks, int hkv,

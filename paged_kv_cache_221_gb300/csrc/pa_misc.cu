@@ -2,6 +2,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+
 #include "pa_ptx.cuh"
 
 namespace pa {
@@ -271,6 +273,28 @@ cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s) {
     splitkv_reduce_kernel<64><<<static_cast<unsigned>(ctas), kMergeWarps * 32, 0, s>>>(p, W);
   else
     splitkv_reduce_kernel<128><<<static_cast<unsigned>(ctas), kMergeWarps * 32, 0, s>>>(p, W);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- graph runner padding
+__global__ void pad_rows_kernel(int32_t* __restrict__ tables, int32_t* __restrict__ lens,
+                                int from, int to, int mbs, int pad_block, int len) {
+  const long long n = static_cast<long long>(to - from) * mbs;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int row = from + static_cast<int>(i / mbs);
+    tables[static_cast<size_t>(row) * mbs + i % mbs] = pad_block;
+    if (i % mbs == 0) lens[row] = len;
+  }
+}
+
+cudaError_t launch_pad_rows(int32_t* block_tables, int32_t* context_lens, int from, int to,
+                            int max_blocks_per_seq, int pad_block, int len, cudaStream_t s) {
+  const long long n = static_cast<long long>(to - from) * max_blocks_per_seq;
+  if (n <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 1024));
+  pad_rows_kernel<<<blocks, 256, 0, s>>>(block_tables, context_lens, from, to,
+                                         max_blocks_per_seq, pad_block, len);
   return cudaGetLastError();
 }
 
