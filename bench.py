@@ -57,6 +57,10 @@ def parse_args():
     ap.add_argument("--partition-size", type=int, default=-1,
                     help="split-KV partition tokens (-1 = the workload's, 0 = library default)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--runner-sweep", action="store_true",
+                    help="per-step latency of small batches: direct calls vs the graph runner")
+    ap.add_argument("--spec-accept", action="store_true",
+                    help="time the speculative acceptance kernel (greedy and sampling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -516,8 +520,131 @@ def run_gb300(args):
         dist.destroy_process_group()
 
 
+def run_runner_sweep(args):
+    """Batches of 1 .. 16 sequences of the 8B-shape decode workload, one token each:
+    the step through the Python binding (host checks + launches) against the same step
+    replayed from the graph runner's class graphs (pad + one graph launch).  Host time
+    per step, measured over many steps with a device synchronisation at the end."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_221_gb300 as pa
+    import workloads as W
+    w = W.FULL["decode_8b"]()
+    dev = torch.device("cuda", 0)
+
+    def td(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.to(dev)
+
+    k, v = td(w.k_cache), td(w.v_cache)
+    used = set(int(x) for x in w.block_tables.ravel() if x >= 0)
+    pad = next(b for b in range(w.num_blocks) if b not in used)
+    mcl, psize = int(w.context_lens.max()), 1536
+    classes = (1, 2, 4, 8, 16)
+    r = pa.GraphRunner(k, v, w.num_q_heads, mcl, w.max_blocks_per_seq, pad, psize,
+                       classes=classes, scale=w.scale)
+    ws = torch.empty(max(pa.workspace_size(16, w.num_q_heads, 1, mcl, 128, 16, psize), 256),
+                     dtype=torch.uint8, device=dev)
+    rows = []
+    for B in range(1, 17):
+        q, tb, ln = td(w.q[:B]), td(w.block_tables[:B]), td(w.context_lens[:B])
+        nk, nv = td(w.new_key[:B]), td(w.new_value[:B])
+        out = torch.empty_like(q)
+        r.q[:B].copy_(q)
+        r.new_key[:B].copy_(nk)
+        r.new_value[:B].copy_(nv)
+        r.block_tables[:B].copy_(tb)
+        r.context_lens[:B].copy_(ln)
+
+        def direct():
+            pa.verify(q, k, v, tb, ln, mcl, w.scale, psize, ws, out, nk, nv)
+
+        def graph():
+            r.step(B)
+
+        res = {"B": B, "class": r.class_of(B)}
+        stream = torch.cuda.current_stream(dev)
+        for name, f in (("direct", direct), ("graph", graph)):
+            for _ in range(20):
+                f()
+            torch.cuda.synchronize(dev)
+            n = 300
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            e0.record(stream)
+            for _ in range(n):
+                f()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            res[name + "_wall_us"] = round((time.perf_counter() - t0) / n * 1e6, 2)
+            res[name + "_device_us"] = round(e0.elapsed_time(e1) / n * 1e3, 2)
+            # host cost alone: issue with the device idle between calls
+            host = 0.0
+            for _ in range(50):
+                torch.cuda.synchronize(dev)
+                h0 = time.perf_counter()
+                f()
+                host += time.perf_counter() - h0
+            res[name + "_host_us"] = round(host / 50 * 1e6, 2)
+        rows.append(res)
+    r.close()
+    print(json.dumps({"metric": "decode step latency, batches of 1-16 (8B shape, one token "
+                                "per sequence)", "unit": "us per step (wall clock with the device "
+                                "kept busy; device time by CUDA events; host issue time with "
+                                "the device idle)",
+                      "classes": list(classes), "partition_size": psize,
+                      "max_context_len": mcl, "rows": rows}), flush=True)
+
+
+def run_spec_accept_timing(args):
+    """The speculative acceptance kernel on random probabilities (uniform drafts)."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_221_gb300 as pa
+    g = torch.Generator(device="cuda").manual_seed(0)
+    rows = []
+    for B, K, V in ((32, 5, 128256), (64, 5, 32000), (8, 8, 151936)):
+        p = torch.rand(B, K + 1, V, device="cuda", generator=g)
+        p /= p.sum(-1, keepdim=True)
+        q = torch.rand(B, K, V, device="cuda", generator=g)
+        q /= q.sum(-1, keepdim=True)
+        d = torch.randint(0, V, (B, K), device="cuda", dtype=torch.int32, generator=g)
+        a = torch.randint(0, 1 << 24, (B, K), device="cuda", dtype=torch.int32, generator=g)
+        s = torch.randint(-(1 << 31), (1 << 31) - 1, (B,), device="cuda", dtype=torch.int32,
+                          generator=g)
+        for greedy in (False, True):
+            def f():
+                pa.spec_accept(p, d, q, a, s, greedy=greedy)
+            for _ in range(5):
+                f()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(50):
+                f()
+            e1.record()
+            e1.synchronize()
+            rows.append({"B": B, "K": K, "V": V, "greedy": greedy,
+                         "us": round(e0.elapsed_time(e1) / 50 * 1000, 1)})
+    print(json.dumps({"metric": "speculative acceptance kernel time", "unit": "us per call",
+                      "rows": rows}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.runner_sweep:
+        run_runner_sweep(args)
+        return
+    if args.spec_accept:
+        run_spec_accept_timing(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
