@@ -98,8 +98,9 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
 /*
  * pa_workspace_size — bytes of scratch the attention calls need for split-KV
  * partials with these sizes (0 if no sequence can need more than one
- * partition).  With partition_size = 0 it sizes for the smallest partition the
- * library default may pick (the default also depends on num_kv_heads), so the
+ * partition).  With partition_size = 0 it returns the largest need of the
+ * library default over every kv-head count that divides num_q_heads (the
+ * default depends on num_kv_heads, which this call does not take), so the
  * result always suffices.  max_prefix_blocks is 0 for pa_decode / pa_verify.
  */
 size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_query_tokens,
@@ -329,8 +330,8 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
  * The split-KV scratch comes from one fixed array of 32 MiB (33554432 bytes)
  * inside this library's device image.  It exists on every GPU the library is
  * loaded on and is held until the process exits.  If the call needs more than
- * 32 MiB (pa_workspace_size with the same sizes, num_query_tokens 1,
- * max_prefix_blocks 0) it returns PA_ERR_WORKSPACE and launches nothing.
+ * 32 MiB (the scratch pa_decode needs with these sizes, num_kv_heads included)
+ * it returns PA_ERR_WORKSPACE and launches nothing.
  * Nothing is allocated by this call or by anything it calls.
  *
  * The first call on each device looks up the array's device address
@@ -418,10 +419,11 @@ pa_status pa_spec_accept(const float* target_probs, const float* draft_probs,
  * c >= B with a one-block dummy sequence (context num_query_tokens, every table
  * entry pad_block, a physical block no sequence uses and that the padded rows'
  * appends may overwrite), then replays graph c on `stream`.  Output rows 0 .. B-1
- * are those of pa_attention with num_seqs = B and the same partition_size.
- * partition_size must be explicit (> 0) so every class splits alike;
- * max_context_len is the bound every captured launch is sized for.  The
- * workspace must hold pa_workspace_size(largest class, ...).  The runner owns
+ * are those of pa_attention with num_seqs = B and the class's partition size:
+ * partition_size if > 0, else the library default for num_seqs = c
+ * (pa_default_partition_size).  max_context_len is the bound every captured
+ * launch is sized for.  The workspace must hold the largest need over the
+ * classes (pa_workspace_size for each class).  The runner owns
  * one CUDA stream (for capture) and the instantiated graphs, nothing else.
  * pa_runner_step returns PA_ERR_UNSUPPORTED when B exceeds the largest class.
  */

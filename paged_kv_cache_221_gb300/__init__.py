@@ -456,7 +456,8 @@ class GraphRunner:
     rows 0 .. B-1 of ``q``, ``new_key``, ``new_value``, ``block_tables`` and
     ``context_lens``, call ``step(B)``, read rows 0 .. B-1 of ``out``.  Rows B .. c-1 of
     the class c are padded on the device with a one-block sequence in ``pad_block`` (a
-    physical block no sequence uses).  ``partition_size`` must be explicit.
+    physical block no sequence uses).  ``partition_size`` 0 captures each class with the
+    library default for its batch size.
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_q_heads: int,
@@ -484,7 +485,8 @@ class GraphRunner:
         self.block_tables = torch.full((Bmax, max_blocks_per_seq), pad_block, dtype=torch.int32,
                                        device=dev)
         self.context_lens = torch.full((Bmax,), T, dtype=torch.int32, device=dev)
-        need = workspace_size(Bmax, num_q_heads, T, max_context_len, D, BS, partition_size, 0)
+        need = max(workspace_size(c, num_q_heads, T, max_context_len, D, BS, partition_size, 0)
+                   for c in classes)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         self._keep = (k_cache, v_cache, k_scale, v_scale)
         self._classes_c = (ctypes.c_int * len(classes))(*classes)

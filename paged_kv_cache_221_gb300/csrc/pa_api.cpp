@@ -84,14 +84,22 @@ struct Plan {
 };
 
 // Partition sizes measured best on GB300: contexts up to 1024 tokens stay
-// whole; up to 4096 tokens, 1536-token partitions; longer contexts, 2048-token
-// partitions, or 3072 when there are many (sequence, kv head) pairs (>= 1024)
-// so that fewer partials need merging.  num_kv_heads = 0 (unknown) gives the
-// smallest of these choices, so a workspace sized with it always suffices.
+// whole.  Few (sequence, kv head) pairs (< 256, small batches): partitions that
+// give about 512 CTAs (1024 above 4096 tokens), at least 128 tokens each, so
+// that a small batch still spreads over the whole GPU.  Otherwise: up to 4096
+// tokens, 1536-token partitions; longer contexts, 2048-token partitions, or
+// 3072 when there are many pairs (>= 1024) so that fewer partials need merging.
 int default_partition_tokens(int max_context_len, int num_seqs, int num_kv_heads) {
   if (max_context_len <= 1024) return ceil_div(max_context_len, kBlockSize) * kBlockSize;
+  const long long pairs = static_cast<long long>(num_seqs) * num_kv_heads;
+  if (pairs > 0 && pairs < 256) {
+    const long long target = max_context_len > 4096 ? 1024 : 512;
+    const long long parts = (target + pairs - 1) / pairs;
+    const int ps = ceil_div(ceil_div(max_context_len, parts), kBlockSize) * kBlockSize;
+    return std::max(ps, 128);
+  }
   if (max_context_len <= 4096) return 1536;
-  if (num_kv_heads > 0 && static_cast<long long>(num_seqs) * num_kv_heads >= 1024) return 3072;
+  if (pairs >= 1024) return 3072;
   return 2048;
 }
 
@@ -285,6 +293,21 @@ pa_status run_attention(const AttnArgs& a) {
 
 }  // namespace
 
+namespace pa {
+
+size_t workspace_for(int num_seqs, int num_q_heads, int num_kv_heads, int num_query_tokens,
+                     int max_context_len, int head_dim, int partition_size,
+                     int max_prefix_blocks) {
+  const int psize = partition_size > 0
+                        ? partition_size
+                        : default_partition_tokens(max_context_len, num_seqs, num_kv_heads);
+  return make_plan(num_seqs, num_q_heads, num_query_tokens, max_context_len, head_dim, psize,
+                   max_prefix_blocks)
+      .ws_bytes;
+}
+
+}  // namespace pa
+
 extern "C" {
 
 const char* pa_status_string(int status) {
@@ -371,12 +394,16 @@ size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_query_tokens,
   if (num_seqs <= 0 || num_q_heads <= 0 || num_query_tokens <= 0 || max_context_len <= 0 ||
       head_dim <= 0 || block_size != kBlockSize || partition_size < 0 || max_prefix_blocks < 0)
     return 0;
-  // num_kv_heads is not known here: size for the smallest default partition
-  const int psize = partition_size == 0 ? default_partition_tokens(max_context_len, num_seqs, 0)
-                                        : partition_size;
-  return make_plan(num_seqs, num_q_heads, num_query_tokens, max_context_len, head_dim, psize,
-                   max_prefix_blocks)
-      .ws_bytes;
+  if (partition_size > 0)
+    return pa::workspace_for(num_seqs, num_q_heads, 1, num_query_tokens, max_context_len,
+                             head_dim, partition_size, max_prefix_blocks);
+  // num_kv_heads is not known here: the largest need over every kv-head count
+  size_t most = 0;
+  for (int h = 1; h <= num_q_heads; ++h)
+    if (num_q_heads % h == 0)
+      most = std::max(most, pa::workspace_for(num_seqs, num_q_heads, h, num_query_tokens,
+                                              max_context_len, head_dim, 0, max_prefix_blocks));
+  return most;
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -51,6 +51,12 @@ struct AttnParams {
   unsigned long long timeout_ns;  // limit of every pipeline wait
 };
 
+// Split-KV scratch bytes a call with these sizes needs (partition_size 0 = the
+// library default for this kv-head count).
+size_t workspace_for(int num_seqs, int num_q_heads, int num_kv_heads, int num_query_tokens,
+                     int max_context_len, int head_dim, int partition_size,
+                     int max_prefix_blocks);
+
 // Kernel launchers (one translation unit per head_dim and mode); `rows` is the
 // number of query rows one CTA carries (1 .. kMaxRows).
 // overlap_previous: launch with programmatic stream serialisation so the kernel may

@@ -52,8 +52,13 @@ extern "C" pa_status pa_decode_static_scratch(
     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
     int max_context_len, int num_seqs, int num_blocks, int num_q_heads, int num_kv_heads,
     int head_dim, int block_size, float scale, int partition_size, pa_stream_t stream) {
-  const size_t need = pa_workspace_size(num_seqs, num_q_heads, 1, max_context_len, head_dim,
-                                        block_size, partition_size, 0);
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len <= 0 ||
+      head_dim <= 0 || block_size != pa::kBlockSize || partition_size < 0)
+    return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                     max_context_len, num_seqs, num_blocks, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, partition_size, nullptr, 0, stream);
+  const size_t need = pa::workspace_for(num_seqs, num_q_heads, num_kv_heads, 1,
+                                        max_context_len, head_dim, partition_size, 0);
   if (need > kStaticScratchBytes) return PA_ERR_WORKSPACE;
   void* ws = nullptr;
   if (need > 0 && scratch_address(&ws) != cudaSuccess) return PA_ERR_CUDA;

@@ -35,6 +35,14 @@ struct pa_graph_runner {
 
 namespace {
 
+// The partition size a class is captured with: the configured one, or the library
+// default for that batch size.
+int partition_for(const pa_runner_config& c, int num_seqs) {
+  return c.partition_size > 0 ? c.partition_size
+                              : pa_default_partition_size(num_seqs, c.num_kv_heads,
+                                                          c.max_context_len, c.block_size);
+}
+
 pa_status attention_for(const pa_graph_runner& r, int num_seqs, cudaStream_t s) {
   const pa_runner_config& c = r.cfg;
   const pa_runner_buffers& b = r.buf;
@@ -42,8 +50,8 @@ pa_status attention_for(const pa_graph_runner& r, int num_seqs, cudaStream_t s) 
                       b.v_scale, c.kv_dtype, c.window_size, b.block_tables,
                       c.max_blocks_per_seq, b.context_lens, c.max_context_len, num_seqs,
                       c.num_query_tokens, c.num_blocks, c.num_q_heads, c.num_kv_heads,
-                      c.head_dim, c.block_size, c.scale, c.partition_size, b.workspace,
-                      b.workspace_bytes, reinterpret_cast<pa_stream_t>(s));
+                      c.head_dim, c.block_size, c.scale, partition_for(c, num_seqs),
+                      b.workspace, b.workspace_bytes, reinterpret_cast<pa_stream_t>(s));
 }
 
 }  // namespace
@@ -54,7 +62,7 @@ pa_status pa_runner_create(const pa_runner_config* cfg, const pa_runner_buffers*
                            pa_graph_runner** out) {
   if (!cfg || !buffers || !out || cfg->num_classes < 1 || !cfg->classes)
     return PA_ERR_INVALID_ARG;
-  if (cfg->partition_size <= 0 || cfg->pad_block < 0 || cfg->pad_block >= cfg->num_blocks ||
+  if (cfg->partition_size < 0 || cfg->pad_block < 0 || cfg->pad_block >= cfg->num_blocks ||
       cfg->num_query_tokens < 1 || cfg->max_context_len < cfg->num_query_tokens)
     return PA_ERR_INVALID_ARG;
   for (int i = 0; i < cfg->num_classes; ++i)

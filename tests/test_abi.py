@@ -52,11 +52,21 @@ def test_workspace_size_host_only(lib):
         return r256(rows * slots * 128 * 4) + r256(rows * slots * 8)
 
     assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 512, 0) == want(8)
-    assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 0, 0) == want(3)   # default 1536
+    # default: the largest need over kv-head counts; one kv head (64 pairs, a small
+    # batch) splits 4096 tokens into 512-token partitions: 8 slots per row
+    assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 0, 0) == want(8)
     assert lib.pa_default_partition_size(64, 8, 4096, 16) == 1536
     assert lib.pa_default_partition_size(64, 8, 100, 16) == 112
     assert lib.pa_default_partition_size(32, 8, 16384, 16) == 2048
     assert lib.pa_default_partition_size(256, 8, 8192, 16) == 3072
+    # small batches (< 256 (sequence, kv head) pairs): about 512 CTAs (1024 above
+    # 4096 tokens), partitions of at least 128 tokens
+    assert lib.pa_default_partition_size(1, 8, 3750, 16) == 128        # 64 parts -> 59 -> 128
+    assert lib.pa_default_partition_size(4, 8, 3750, 16) == 240        # 16 parts
+    assert lib.pa_default_partition_size(8, 8, 3750, 16) == 480        # 8 parts
+    assert lib.pa_default_partition_size(16, 8, 3750, 16) == 944       # 4 parts
+    assert lib.pa_default_partition_size(16, 8, 7850, 16) == 992       # 8 parts (1024 CTAs)
+    assert lib.pa_default_partition_size(1, 8, 900, 16) == 912         # short: whole
     # shared prefix always needs scratch
     assert lib.pa_workspace_size(2, 4, 1, 64, 64, 16, 64, 2) > 0
 

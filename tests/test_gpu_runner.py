@@ -87,6 +87,31 @@ def test_padded_replays_match_direct_calls(T):
     r.close()
 
 
+def test_default_partition_per_class():
+    """partition_size 0: each class is captured with the library default for its size, and
+    a padded replay equals a direct call made with that class's default."""
+    w = make(T=1, n=16, seed=44)
+    mcl = int(w.context_lens.max())
+    k, v = to_dev(w.k_cache), to_dev(w.v_cache)
+    r = pa.GraphRunner(k, v, w.num_q_heads, mcl, w.max_blocks_per_seq, pad_block_of(w), 0,
+                       classes=(1, 4, 16), scale=w.scale)
+    for B in (1, 3, 16):
+        c = r.class_of(B)
+        psize = pa.default_partition_size(c, w.num_kv_heads, mcl)
+        q, nk, nv, tb, ln, slots = sub(w, B)
+        r.q[:B].copy_(to_dev(q))
+        r.new_key[:B].copy_(to_dev(nk))
+        r.new_value[:B].copy_(to_dev(nv))
+        r.block_tables[:B].copy_(to_dev(tb))
+        r.context_lens[:B].copy_(to_dev(ln))
+        r.step(B)
+        k2, v2 = to_dev(w.k_cache), to_dev(w.v_cache)
+        want = pa.attention(to_dev(q), k2, v2, to_dev(tb), to_dev(ln), mcl, w.scale, psize,
+                            new_key=to_dev(nk), new_value=to_dev(nv))
+        assert torch.equal(r.out[:B].view(torch.int16), want.view(torch.int16)), f"B={B}"
+    r.close()
+
+
 def test_runner_with_window_and_fp8_pages():
     base = make(T=2, n=8, seed=5)
     w = W.fp8_variant(base, seed=2)
@@ -114,6 +139,6 @@ def test_bad_configuration_rejected():
     w = make(n=2)
     k, v = to_dev(w.k_cache), to_dev(w.v_cache)
     with pytest.raises(pa.PagedAttnError):
-        pa.GraphRunner(k, v, 32, 900, w.max_blocks_per_seq, 0, 0)        # partition_size 0
+        pa.GraphRunner(k, v, 32, 900, w.max_blocks_per_seq, 0, -16)      # partition_size < 0
     with pytest.raises(pa.PagedAttnError):
         pa.GraphRunner(k, v, 32, 900, w.max_blocks_per_seq, w.num_blocks, 256)  # pad block
