@@ -30,8 +30,8 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "paged decode-attention KV-read GB/s vs GB300 HBM peak; seq-steps/sec"
-KERNEL_SOURCES = ["pa_attn.cuh", "pa_ptx.cuh", "pa_internal.h", "attn_d128.cu", "pa_misc.cu",
-                  "group_d128.cu", "attn8_d128.cu"]
+KERNEL_SOURCES = ["pa_attn.cuh", "pa_ptx.cuh"]   # the attention kernel template and its PTX
+KERNEL_PARAMS = "pa_internal.h"                  # its constants and AttnParams (up to the struct end)
 WORKLOAD_DESC = {
     "tiny": "2 seqs (ctx 37, 100), 4 q = 4 kv heads, head_dim 64, 16-block pool",
     "decode_8b": "64 seqs, ctx uniform [512, 4096], 32 q / 8 kv heads, head_dim 128",
@@ -52,8 +52,7 @@ def parse_args():
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window (positions each query token sees); 0 = none")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
-                    help="KV page format (fp8 = E4M3 pages with per-kv-head scales; the "
-                         "per-sequence path)")
+                    help="KV page format (fp8 = E4M3 pages with per-kv-head scales)")
     ap.add_argument("--partition-size", type=int, default=-1,
                     help="split-KV partition tokens (-1 = the workload's, 0 = library default)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -106,10 +105,17 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of what the attention kernel is compiled from: its template, its PTX helpers,
+    and the constants and parameter struct it reads (launcher declarations excluded)."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_221_gb300", "csrc")
     h = hashlib.sha256()
     for n in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_221_gb300", "csrc", n), "rb") as f:
+        with open(os.path.join(csrc, n), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(csrc, KERNEL_PARAMS), "rb") as f:
+        text = f.read()
+    end = text.find(b"};", text.find(b"struct AttnParams"))
+    h.update(text[:end + 2])
     return h.hexdigest()[:16]
 
 
@@ -201,7 +207,7 @@ def workload_config(w, ps, world, window=0):
     base = w.name[:-4] if w.name.endswith("_fp8") else w.name
     desc = WORKLOAD_DESC.get(base, base)
     if w.kv_dtype == "fp8":
-        desc += "; FP8 (E4M3) K/V pages, per-kv-head scales, per-sequence path"
+        desc += "; FP8 (E4M3) K/V pages, per-kv-head scales"
     if window > 0:
         desc += f"; sliding window of {window} positions (only the pages under the windows " \
                 f"are read and counted)"
@@ -311,8 +317,6 @@ def run_gb300(args):
     fp8 = args.kv_dtype == "fp8"
     if fp8:
         import workloads as W
-        w.seq_group = None                  # FP8 pages run the per-sequence path
-        w.group_prefix_blocks = None
         w = W.fp8_variant(w, seed=rank)
     if args.window > 0:
         w.seq_group = None                  # the window runs the per-sequence path
@@ -343,19 +347,22 @@ def run_gb300(args):
     # Per-sequence workloads: one fused call (reshape_and_cache inside the attention
     # launch).  Shared-prefix workload: reshape_and_cache, then the shared-prefix call.
     def reshape():
-        if grouped:
+        if grouped and fp8:
+            pa.reshape_and_cache_fp8(nk, nv, k, v, slots, ks, vs)
+        elif grouped:
             pa.reshape_and_cache(nk, nv, k, v, slots)
 
     def attend():
         if args.window > 0:
             pa.attention(q, k, v, tables, lens, w.max_context_len, w.scale, ps, ws, out, nk, nv,
                          window_size=args.window, k_scale=ks, v_scale=vs)
+        elif grouped:
+            pa.decode_shared_prefix(q, k, v, tables, lens, sg, gp, w.max_group_size,
+                                    w.max_prefix_blocks, w.max_context_len, w.scale, ps, ws, out,
+                                    k_scale=ks, v_scale=vs)
         elif fp8:
             pa.verify_fp8(q, k, v, ks, vs, tables, lens, w.max_context_len, w.scale, ps, ws, out,
                           nk, nv)
-        elif grouped:
-            pa.decode_shared_prefix(q, k, v, tables, lens, sg, gp, w.max_group_size,
-                                    w.max_prefix_blocks, w.max_context_len, w.scale, ps, ws, out)
         else:
             pa.verify(q, k, v, tables, lens, w.max_context_len, w.scale, ps, ws, out,
                       nk, nv)

@@ -321,6 +321,22 @@ pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
                                   void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_shared_prefix_fp8 — pa_decode_shared_prefix over FP8 (E4M3) pages
+ * and per-kv-head scales, laid out as for pa_decode_fp8: the group's prefix
+ * pages are read once per group, the private pages once per sequence.
+ * Arguments, requirements and errors as pa_decode_shared_prefix, plus k_scale
+ * and v_scale non-NULL.
+ */
+pa_status pa_decode_shared_prefix_fp8(
+    void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+    const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len, int num_seqs, int num_blocks,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+    int partition_size, const int32_t* seq_group, const int32_t* group_prefix_blocks,
+    int num_groups, int max_group_size, int max_prefix_blocks, void* workspace,
+    size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_static_scratch — pa_decode without caller-provided scratch, for
  * callers that may not allocate device memory: a plugin that its host runtime
  * gives only input and output buffers, or a server that reserves all device

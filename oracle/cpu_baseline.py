@@ -9,7 +9,7 @@ BLAS thread count can be pinned before NumPy loads:
 prints one JSON object: KV bytes read by the oracle (unique pages of the
 sequences it processed), seconds, GB/s and the sample description.  A name
 ending in ``_fp8`` times the FP8-page oracle on that workload's FP8 variant
-(the per-sequence path, variant seed 0).  The
+(variant seed 0).  The
 workload's new tokens are scattered into the caches before timing; the timed
 work is the oracle's paged attention over whole sequences, in batch order,
 repeated over the batch until ``seconds`` have elapsed.
@@ -41,10 +41,7 @@ def threads_used() -> int:
 
 def prepare(name: str):
     if name.endswith("_fp8"):
-        w = W.FULL[name[:-4]]()
-        w.seq_group = None
-        w.group_prefix_blocks = None
-        w = W.fp8_variant(w, seed=0)
+        w = W.fp8_variant(W.FULL[name[:-4]](), seed=0)
         k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
                                    w.k_scale, w.v_scale, w.block_size)
         return w, k, v

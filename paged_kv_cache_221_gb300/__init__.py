@@ -355,13 +355,33 @@ def decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
                          max_group_size: int, max_prefix_blocks: int,
                          max_context_len: Optional[int] = None, scale: Optional[float] = None,
                          partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
-                         out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Decode where groups of sequences share copy-on-write prefix blocks, read once per group."""
+                         out: Optional[torch.Tensor] = None, k_scale: Optional[torch.Tensor] = None,
+                         v_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode where groups of sequences share copy-on-write prefix blocks, read once per group.
+
+    With ``k_scale`` / ``v_scale`` the pools are FP8 (E4M3) pages as for ``decode_fp8``."""
     squeeze = q.dim() == 3
     q4 = q.unsqueeze(1) if squeeze else q
     o4 = None if out is None else (out.unsqueeze(1) if squeeze else out)
-    dev, B, T, Hq, D, NB, Hkv, BS, mcl, o4 = _attn_common(q4, k_cache, v_cache, block_tables,
-                                                         context_lens, max_context_len, o4)
+    fp8 = k_scale is not None
+    if fp8:
+        dev, NB, Hkv, BS, D = _fp8_pools(k_cache, v_cache, k_scale, v_scale)
+        _need("q", q4, torch.bfloat16, 4, dev)
+        _need("block_tables", block_tables, torch.int32, 2, dev)
+        _need("context_lens", context_lens, torch.int32, 1, dev)
+        B, T, Hq, Dq = q4.shape
+        if Dq != D or block_tables.shape[0] != B or context_lens.shape[0] != B:
+            raise ValueError("inconsistent shapes")
+        if max_context_len is None:
+            max_context_len = int(context_lens.max().item()) if B else T   # host sync
+        mcl = int(max_context_len)
+        if o4 is None:
+            o4 = torch.empty_like(q4)
+        else:
+            _need("out", o4, torch.bfloat16, 4, dev)
+    else:
+        dev, B, T, Hq, D, NB, Hkv, BS, mcl, o4 = _attn_common(q4, k_cache, v_cache, block_tables,
+                                                             context_lens, max_context_len, o4)
     if T != 1:
         raise ValueError("decode_shared_prefix takes one query token per sequence")
     _need("seq_group", seq_group, torch.int32, 1, dev)
@@ -369,6 +389,15 @@ def decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     need = workspace_size(B, Hq, 1, mcl, D, BS, partition_size, max_prefix_blocks) if B else 0
     ws, wsb = _workspace(dev, workspace, need)
+    if fp8:
+        st = library().pa_decode_shared_prefix_fp8(
+            _vp(o4), _vp(q4), _vp(k_cache), _vp(v_cache), _vp(k_scale), _vp(v_scale),
+            _vp(block_tables), block_tables.shape[1], _vp(context_lens), mcl, B, NB, Hq, Hkv, D,
+            BS, scale, partition_size, _vp(seq_group), _vp(group_prefix_blocks),
+            group_prefix_blocks.shape[0], max_group_size, max_prefix_blocks, _vp(ws), wsb,
+            _stream(dev))
+        _lib.check("pa_decode_shared_prefix_fp8", st)
+        return o4.squeeze(1) if squeeze else o4
     st = library().pa_decode_shared_prefix(
         _vp(o4), _vp(q4), _vp(k_cache), _vp(v_cache), _vp(block_tables), block_tables.shape[1],
         _vp(context_lens), mcl, B, NB, Hq, Hkv, D, BS, scale, partition_size, _vp(seq_group),

@@ -53,6 +53,9 @@ SIGNATURES = {
                               _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "pa_decode_shared_prefix": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                      _i, _f, _i, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+    "pa_decode_shared_prefix_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i,
+                                         _i, _i, _i, _i, _f, _i, _vp, _vp, _i, _i, _i, _vp, _sz,
+                                         _vp]),
     "pa_decode_static_scratch": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
                                       _i, _i, _f, _i, _vp]),
     "pa_copy_blocks": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),

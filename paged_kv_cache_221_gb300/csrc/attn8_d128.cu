@@ -5,8 +5,8 @@
 namespace pa {
 
 cudaError_t launch_attn8_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                              int rows, dim3 grid, cudaStream_t s) {
-  return launch_dispatch<128, false, true>(tk, tv, p, rows, grid, s, false);
+                              int rows, dim3 grid, cudaStream_t s, bool overlap_previous) {
+  return launch_dispatch<128, false, true>(tk, tv, p, rows, grid, s, overlap_previous);
 }
 
 cudaError_t take_error_attn8_d128(unsigned* bits) { return take_error_word(bits); }

@@ -170,10 +170,7 @@ pa_status run_attention(const AttnArgs& a) {
   const long long rows = static_cast<long long>(a.num_blocks) * a.hkv * kBlockSize;
   if (rows >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
   const bool grouped = a.num_groups > 0;
-  if (a.kv8) {
-    if (!a.k_scale || !a.v_scale) return PA_ERR_INVALID_ARG;
-    if (grouped) return PA_ERR_UNSUPPORTED;
-  }
+  if (a.kv8 && (!a.k_scale || !a.v_scale)) return PA_ERR_INVALID_ARG;
   if (a.window < 0) return PA_ERR_INVALID_ARG;
   if (a.window > 0 && grouped) return PA_ERR_UNSUPPORTED;
   if (grouped) {
@@ -260,8 +257,12 @@ pa_status run_attention(const AttnArgs& a) {
     if (gz > 65535) return PA_ERR_UNSUPPORTED;
     const int rows = mc * G * a.T;
     dim3 grid(ceil_div(a.max_prefix_blocks, plan.ppb), a.hkv, static_cast<unsigned>(gz));
-    e = a.head_dim == 64 ? launch_attn_group_d64(tk, tv, p, rows, grid, a.stream)
-                         : launch_attn_group_d128(tk, tv, p, rows, grid, a.stream);
+    if (a.kv8)
+      e = a.head_dim == 64 ? launch_attn_group8_d64(tk, tv, p, rows, grid, a.stream)
+                           : launch_attn_group8_d128(tk, tv, p, rows, grid, a.stream);
+    else
+      e = a.head_dim == 64 ? launch_attn_group_d64(tk, tv, p, rows, grid, a.stream)
+                           : launch_attn_group_d128(tk, tv, p, rows, grid, a.stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   {
@@ -277,8 +278,8 @@ pa_status run_attention(const AttnArgs& a) {
     if (units >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(units), 1, 1);
     if (a.kv8)
-      e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream)
-                           : launch_attn8_d128(tk, tv, p, rows, grid, a.stream);
+      e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream, group_launch)
+                           : launch_attn8_d128(tk, tv, p, rows, grid, a.stream, group_launch);
     else
       e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                            : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);
@@ -553,6 +554,23 @@ pa_status pa_spec_accept(const float* target_probs, const float* draft_probs,
              : PA_ERR_CUDA;
 }
 
+pa_status pa_decode_shared_prefix_fp8(
+    void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+    const float* v_scale, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len, int num_seqs, int num_blocks,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+    int partition_size, const int32_t* seq_group, const int32_t* group_prefix_blocks,
+    int num_groups, int max_group_size, int max_prefix_blocks, void* workspace,
+    size_t workspace_bytes, pa_stream_t stream) {
+  if (num_groups < 0) return PA_ERR_INVALID_ARG;
+  AttnArgs a{out, q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks_per_seq,
+             context_lens, max_context_len, num_seqs, 1, num_blocks, num_q_heads, num_kv_heads,
+             head_dim, block_size, scale, partition_size, seq_group, group_prefix_blocks,
+             num_groups, max_group_size, max_prefix_blocks, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), true, k_scale, v_scale};
+  return run_attention(a);
+}
+
 pa_status pa_get_device_error(pa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
@@ -560,7 +578,8 @@ pa_status pa_get_device_error(pa_stream_t stream) {
   if (take_error_attn_d64(&bits) != cudaSuccess || take_error_attn_d128(&bits) != cudaSuccess ||
       take_error_group_d64(&bits) != cudaSuccess ||
       take_error_group_d128(&bits) != cudaSuccess || take_error_attn8_d64(&bits) != cudaSuccess ||
-      take_error_attn8_d128(&bits) != cudaSuccess || take_error_spec(&bits) != cudaSuccess ||
+      take_error_attn8_d128(&bits) != cudaSuccess || take_error_group8_d64(&bits) != cudaSuccess ||
+      take_error_group8_d128(&bits) != cudaSuccess || take_error_spec(&bits) != cudaSuccess ||
       take_error_misc(&bits) != cudaSuccess)
     return PA_ERR_CUDA;
   if (bits & kErrTimeout) return PA_ERR_TIMEOUT;

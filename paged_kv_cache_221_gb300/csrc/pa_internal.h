@@ -71,9 +71,13 @@ cudaError_t launch_attn_group_d128(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
 // FP8 (E4M3) pages: K [NB, Hkv, 16, D] token-major, V [NB, Hkv, D, 16] per-page transposed.
 cudaError_t launch_attn8_d64(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                             int rows, dim3 grid, cudaStream_t s);
+                             int rows, dim3 grid, cudaStream_t s, bool overlap_previous);
 cudaError_t launch_attn8_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                              int rows, dim3 grid, cudaStream_t s);
+                              int rows, dim3 grid, cudaStream_t s, bool overlap_previous);
+cudaError_t launch_attn_group8_d64(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
+cudaError_t launch_attn_group8_d128(const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
 cudaError_t launch_reshape_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
                                const int64_t* slots, const float* k_scale, const float* v_scale,
                                int num_tokens, int num_blocks, int hkv, int head_dim,
@@ -103,6 +107,8 @@ cudaError_t take_error_group_d64(unsigned* bits);
 cudaError_t take_error_group_d128(unsigned* bits);
 cudaError_t take_error_attn8_d64(unsigned* bits);
 cudaError_t take_error_attn8_d128(unsigned* bits);
+cudaError_t take_error_group8_d64(unsigned* bits);
+cudaError_t take_error_group8_d128(unsigned* bits);
 cudaError_t take_error_spec(unsigned* bits);
 cudaError_t take_error_misc(unsigned* bits);
 

@@ -245,6 +245,28 @@ def test_append_edge_lengths(D):
     np.testing.assert_array_equal(codes(d.v), vref)
 
 
+def shared_fp8(size="small"):
+    base = (W.SMALL if size == "small" else W.FULL)["shared_prefix"]()
+    return W.fp8_variant(base, seed=13)
+
+
+@pytest.mark.parametrize("psize", [128, 256, 0])
+def test_shared_prefix_read_once(psize):
+    """FP8 pages through the shared-prefix call: matches the oracle, and matches the
+    per-sequence FP8 call within tolerance."""
+    w = shared_fp8()
+    ref, _, _ = F.run_workload(w)
+    d = Dev8(w)
+    d.reshape()
+    sg, gp = to_dev(w.seq_group), to_dev(w.group_prefix_blocks)
+    out = pa.decode_shared_prefix(d.q, d.k, d.v, d.tables, d.lens, sg, gp, w.max_group_size,
+                                  w.max_prefix_blocks, w.max_context_len, w.scale, psize,
+                                  k_scale=d.ks, v_scale=d.vs)
+    assert_close(out, ref, what=f"fp8 shared prefix ps{psize}")
+    plain = d.attend(partition_size=psize)
+    assert_close(out, plain.float().cpu().double().numpy(), what="fp8 shared vs plain")
+
+
 def sample_seqs(w, n=6, seed=0):
     L = w.context_lens
     pick = {int(np.argmin(L)), int(np.argmax(L))}
