@@ -264,71 +264,86 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     constexpr int GP = Gm::kIssueGroup;
     static_assert(GP >= 1 && GP <= NS && 32 % GP == 0, "issue group");
     bool aborted = false;
+    // Query tokens' K/V that land in this unit's pages are stored into the pool
+    // first (reshape_and_cache fused; FP8 pages quantise on the way).  The stores
+    // are issued once the first group of pages is in flight (before it, if that
+    // group holds a new token), and the proxy fence only right before the first
+    // page that holds a new token is issued, so the stores have long landed and
+    // neither the stores nor the fence stall the stream.
+    int fence_at = npages;                    // first unit page that holds a new token
+    int jlo = npages, jhi = -1;               // unit pages that hold new tokens
+    if constexpr (!GROUP) {
+      if (p.new_k != nullptr) {
+        jlo = max(0, (vlen - T) / kBlockSize - pg0);
+        jhi = min(npages - 1, (vlen - 1) / kBlockSize - pg0);
+      }
+    }
+    bool pending = jlo <= jhi;
+    auto store_new_tokens = [&]() {
+      for (int j = jlo; j <= jhi; ++j) {
+        const int phys = __ldg(trow + pg0 + j);
+        const int pos0 = (pg0 + j) * kBlockSize;
+        const int lo = max(vlen - T, pos0), hi = min(vlen - 1, pos0 + kBlockSize - 1);
+        if (lo > hi || static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks))
+          continue;                           // out-of-range ids are reported when issued
+        fence_at = min(fence_at, j);
+        for (int pos = lo; pos <= hi; ++pos) {
+          const size_t src = (static_cast<size_t>(b_single) * T + (pos - (vlen - T))) * p.Hkv + g;
+          const size_t page = static_cast<size_t>(phys) * p.Hkv + g;
+          const int off = pos & (kBlockSize - 1);
+          if constexpr (KV8) {
+            // lane c: head dims 4c .. 4c+3; K row bytes contiguous, V bytes one per
+            // transposed row
+            const float ks = p.k_scale[g], vs = p.v_scale[g];
+            for (int c = lane; c < D / 4; c += 32) {
+              const uint2 kx = reinterpret_cast<const uint2*>(p.new_k)[src * (D / 4) + c];
+              const uint2 vx = reinterpret_cast<const uint2*>(p.new_v)[src * (D / 4) + c];
+              const uint32_t k01 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(kx.x), ks),
+                                                   __fdiv_rn(bf16_hi(kx.x), ks));
+              const uint32_t k23 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(kx.y), ks),
+                                                   __fdiv_rn(bf16_hi(kx.y), ks));
+              const uint32_t v01 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(vx.x), vs),
+                                                   __fdiv_rn(bf16_hi(vx.x), vs));
+              const uint32_t v23 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(vx.y), vs),
+                                                   __fdiv_rn(bf16_hi(vx.y), vs));
+              uint8_t* kp = static_cast<uint8_t*>(p.k_pool);
+              uint8_t* vp = static_cast<uint8_t*>(p.v_pool);
+              *reinterpret_cast<uint32_t*>(kp + (page * kBlockSize + off) * D + 4 * c) =
+                  k01 | (k23 << 16);
+              uint8_t* vrow = vp + (page * D + 4 * c) * kBlockSize + off;
+              vrow[0] = static_cast<uint8_t>(v01 & 0xFFu);
+              vrow[kBlockSize] = static_cast<uint8_t>(v01 >> 8);
+              vrow[2 * kBlockSize] = static_cast<uint8_t>(v23 & 0xFFu);
+              vrow[3 * kBlockSize] = static_cast<uint8_t>(v23 >> 8);
+            }
+          } else {
+            constexpr int CH = D / 8;           // 16-byte chunks per row
+            const size_t dst = page * kBlockSize + off;
+            for (int c = lane; c < 2 * CH; c += 32) {
+              const bool isv = c >= CH;
+              const int cc = isv ? c - CH : c;
+              const uint4 v =
+                  reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + cc];
+              reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + cc] = v;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      pending = false;
+    };
+    if (pending && jlo < GP) store_new_tokens();   // the first group holds a new token
     for (int base = 0; base < npages; base += 32) {
       const int phys_l = base == 0 ? phys_first
                                    : ((base + lane < npages) ? __ldg(trow + pg0 + base + lane) : 0);
       const int cnt = min(32, npages - base);
       for (int j0 = 0; j0 < cnt; j0 += GP) {
         const int jn = min(j0 + GP, cnt);
-        if constexpr (!GROUP) {
-          // Query tokens' K/V that land in these pages are stored into the pool
-          // first (reshape_and_cache fused; FP8 pages quantise on the way), then
-          // the pages are read by TMA.
-          if (p.new_k != nullptr) {
-            bool wrote = false;                 // warp-uniform
-            for (int j = j0; j < jn; ++j) {
-              const int phys = __shfl_sync(0xffffffffu, phys_l, j);
-              const int pos0 = (pg0 + base + j) * kBlockSize;
-              const int lo = max(vlen - T, pos0), hi = min(vlen - 1, pos0 + kBlockSize - 1);
-              if (lo > hi || static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks))
-                continue;
-              for (int pos = lo; pos <= hi; ++pos) {
-                const size_t src =
-                    (static_cast<size_t>(b_single) * T + (pos - (vlen - T))) * p.Hkv + g;
-                const size_t page = static_cast<size_t>(phys) * p.Hkv + g;
-                const int off = pos & (kBlockSize - 1);
-                if constexpr (KV8) {
-                  // lane c: head dims 4c .. 4c+3; K row bytes contiguous, V bytes
-                  // one per transposed row
-                  const float ks = p.k_scale[g], vs = p.v_scale[g];
-                  for (int c = lane; c < D / 4; c += 32) {
-                    const uint2 kx = reinterpret_cast<const uint2*>(p.new_k)[src * (D / 4) + c];
-                    const uint2 vx = reinterpret_cast<const uint2*>(p.new_v)[src * (D / 4) + c];
-                    const uint32_t k01 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(kx.x), ks),
-                                                         __fdiv_rn(bf16_hi(kx.x), ks));
-                    const uint32_t k23 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(kx.y), ks),
-                                                         __fdiv_rn(bf16_hi(kx.y), ks));
-                    const uint32_t v01 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(vx.x), vs),
-                                                         __fdiv_rn(bf16_hi(vx.x), vs));
-                    const uint32_t v23 = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(vx.y), vs),
-                                                         __fdiv_rn(bf16_hi(vx.y), vs));
-                    uint8_t* kp = static_cast<uint8_t*>(p.k_pool);
-                    uint8_t* vp = static_cast<uint8_t*>(p.v_pool);
-                    *reinterpret_cast<uint32_t*>(kp + (page * kBlockSize + off) * D + 4 * c) =
-                        k01 | (k23 << 16);
-                    uint8_t* vrow = vp + (page * D + 4 * c) * kBlockSize + off;
-                    vrow[0] = static_cast<uint8_t>(v01 & 0xFFu);
-                    vrow[kBlockSize] = static_cast<uint8_t>(v01 >> 8);
-                    vrow[2 * kBlockSize] = static_cast<uint8_t>(v23 & 0xFFu);
-                    vrow[3 * kBlockSize] = static_cast<uint8_t>(v23 >> 8);
-                  }
-                } else {
-                  constexpr int CH = D / 8;     // 16-byte chunks per row
-                  const size_t dst = page * kBlockSize + off;
-                  for (int c = lane; c < 2 * CH; c += 32) {
-                    const bool isv = c >= CH;
-                    const int cc = isv ? c - CH : c;
-                    const uint4 v =
-                        reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + cc];
-                    reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + cc] = v;
-                  }
-                }
-              }
-              wrote = true;
-            }
-            if (wrote) fence_proxy_async_global();
-            __syncwarp();
-          }
+        if (base + jn > fence_at) {
+          // the stores must be visible to the TMA reads of the pages that hold them
+          fence_proxy_async_global();
+          __syncwarp();
+          fence_at = npages;
         }
         if (lane >= j0 && lane < jn) {
           const int it = base + lane;
@@ -362,6 +377,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
         }
         // a wait that gave up on any lane ends the streaming of the whole warp
         aborted = __any_sync(0xffffffffu, aborted);
+        if (pending) store_new_tokens();            // the first group is in flight
       }
     }
     // Do not leave while copies issued by this warp may still be landing.
