@@ -467,6 +467,24 @@ typedef struct pa_runner_buffers {   /* device pointers, as for pa_attention */
   const float* v_scale;
   void* workspace;
   size_t workspace_bytes;
+  /* Optional host staging (page-locked host memory, same shapes as the device
+   * buffers above; all NULL = none).  With staging every class graph also holds
+   * the copies of its c rows of q, new_key, new_value, block_tables and
+   * context_lens from these buffers to the device buffers before the attention
+   * call, and the copy of c rows of out back to h_out after it; pa_runner_step
+   * then pads host rows B .. c-1 of h_block_tables / h_context_lens on the CPU
+   * instead of launching the padding kernel.  When the five host inputs and the
+   * five device inputs each lie in one range, in the order q, new_key,
+   * new_value, block_tables, context_lens and at the same offsets, the graph
+   * copies that whole range (sized for the largest class) in one piece.  Read
+   * h_out, and rewrite the host
+   * inputs for the next step, only after the stream has finished the step. */
+  void* h_q;
+  void* h_new_key;
+  void* h_new_value;
+  int32_t* h_block_tables;
+  int32_t* h_context_lens;
+  void* h_out;
 } pa_runner_buffers;
 
 typedef struct pa_graph_runner pa_graph_runner;

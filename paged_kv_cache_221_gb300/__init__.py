@@ -27,6 +27,7 @@ import ctypes
 import math
 from typing import Optional
 
+import numpy as np
 import torch
 
 from . import _lib
@@ -487,13 +488,19 @@ class GraphRunner:
     the class c are padded on the device with a one-block sequence in ``pad_block`` (a
     physical block no sequence uses).  ``partition_size`` 0 captures each class with the
     library default for its batch size.
+
+    With ``host_staging`` the runner also allocates page-locked host mirrors ``h_q``,
+    ``h_new_key``, ``h_new_value``, ``h_block_tables``, ``h_context_lens`` and ``h_out``,
+    and every class graph copies the inputs in and the output back itself: write the
+    step's inputs into the host rows, call ``step(B)``, synchronise, read ``h_out``.
     """
 
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_q_heads: int,
                  max_context_len: int, max_blocks_per_seq: int, pad_block: int,
                  partition_size: int, classes=(1, 2, 4, 8, 16), num_query_tokens: int = 1,
                  scale: Optional[float] = None, window_size: int = 0, fused_append: bool = True,
-                 k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
+                 k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                 host_staging: bool = False):
         self._lib = library()
         fp8 = k_scale is not None
         if fp8:
@@ -506,18 +513,52 @@ class GraphRunner:
         classes = sorted(int(c) for c in classes)
         Bmax, T = classes[-1], int(num_query_tokens)
         self.classes = classes
-        self.q = torch.zeros((Bmax, T, num_q_heads, D), dtype=torch.bfloat16, device=dev)
+        # the inputs live in one block (q, new_key, new_value, block_tables, context_lens,
+        # 256-byte aligned), mirrored on the host when staging, so one copy moves them all
+        shapes = [("q", (Bmax, T, num_q_heads, D), torch.bfloat16),
+                  ("new_key", (Bmax * T, Hkv, D), torch.bfloat16),
+                  ("new_value", (Bmax * T, Hkv, D), torch.bfloat16),
+                  ("block_tables", (Bmax, max_blocks_per_seq), torch.int32),
+                  ("context_lens", (Bmax,), torch.int32)]
+        offs, total = [], 0
+        for _, shp, dt in shapes:
+            offs.append(total)
+            n = int(np.prod(shp)) * torch.tensor([], dtype=dt).element_size()
+            total += (n + 255) // 256 * 256
+
+        def carve(block):
+            return {name: block[o:o + int(np.prod(shp)) * torch.tensor([], dtype=dt)
+                                .element_size()].view(dt).view(shp)
+                    for (name, shp, dt), o in zip(shapes, offs)}
+
+        self._dblock = torch.zeros(total, dtype=torch.uint8, device=dev)
+        d = carve(self._dblock)
+        self.q, self.block_tables, self.context_lens = d["q"], d["block_tables"], d["context_lens"]
+        self.new_key = d["new_key"] if fused_append else None
+        self.new_value = d["new_value"] if fused_append else None
+        self.block_tables.fill_(pad_block)
+        self.context_lens.fill_(T)
         self.out = torch.zeros_like(self.q)
-        self.new_key = torch.zeros((Bmax * T, Hkv, D), dtype=torch.bfloat16, device=dev) \
-            if fused_append else None
-        self.new_value = torch.zeros_like(self.new_key) if fused_append else None
-        self.block_tables = torch.full((Bmax, max_blocks_per_seq), pad_block, dtype=torch.int32,
-                                       device=dev)
-        self.context_lens = torch.full((Bmax,), T, dtype=torch.int32, device=dev)
         need = max(workspace_size(c, num_q_heads, T, max_context_len, D, BS, partition_size, 0)
                    for c in classes)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         self._keep = (k_cache, v_cache, k_scale, v_scale)
+        host = None
+        if host_staging:
+            self._hblock = torch.zeros(total, dtype=torch.uint8).pin_memory()
+            hb = carve(self._hblock)
+            self.h_q, self.h_block_tables = hb["q"], hb["block_tables"]
+            self.h_context_lens = hb["context_lens"]
+            self.h_new_key = hb["new_key"] if fused_append else None
+            self.h_new_value = hb["new_value"] if fused_append else None
+            self.h_block_tables.fill_(pad_block)
+            self.h_context_lens.fill_(T)
+            self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+            host = (self.h_q.data_ptr(),
+                    self.h_new_key.data_ptr() if fused_append else None,
+                    self.h_new_value.data_ptr() if fused_append else None,
+                    self.h_block_tables.data_ptr(), self.h_context_lens.data_ptr(),
+                    self.h_out.data_ptr())
         self._classes_c = (ctypes.c_int * len(classes))(*classes)
         cfg = _lib.RunnerConfig(num_q_heads, Hkv, D, BS, T, max_blocks_per_seq, max_context_len,
                                 NB, 1 if fp8 else 0, int(window_size), int(partition_size),
@@ -531,7 +572,7 @@ class GraphRunner:
                                   k_scale.data_ptr() if fp8 else None,
                                   v_scale.data_ptr() if fp8 else None,
                                   self.workspace.data_ptr(),
-                                  self.workspace.numel())
+                                  self.workspace.numel(), *(host or (None,) * 6))
         h = ctypes.c_void_p()
         torch.cuda.synchronize(dev)
         _lib.check("pa_runner_create", self._lib.pa_runner_create(ctypes.byref(cfg),

@@ -34,7 +34,9 @@ class RunnerBuffers(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("out", "q", "new_key", "new_value",
                                                  "block_tables", "context_lens", "k_cache",
                                                  "v_cache", "k_scale", "v_scale", "workspace")] + \
-               [("workspace_bytes", ctypes.c_size_t)]
+               [("workspace_bytes", ctypes.c_size_t)] + \
+               [(n, ctypes.c_void_p) for n in ("h_q", "h_new_key", "h_new_value",
+                                                 "h_block_tables", "h_context_lens", "h_out")]
 
 
 # Every symbol the header declares, with (restype, argtypes).

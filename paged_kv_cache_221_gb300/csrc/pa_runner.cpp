@@ -43,15 +43,69 @@ int partition_for(const pa_runner_config& c, int num_seqs) {
                                                           c.max_context_len, c.block_size);
 }
 
-pa_status attention_for(const pa_graph_runner& r, int num_seqs, cudaStream_t s) {
+bool staged(const pa_runner_buffers& b) {
+  return b.h_q && b.h_block_tables && b.h_context_lens && b.h_out &&
+         (b.new_key == nullptr || (b.h_new_key && b.h_new_value));
+}
+
+// When the host inputs and the device inputs each form one range, in the same
+// order and at the same offsets (q, new_key, new_value, block_tables,
+// context_lens), the bytes of that range for the largest class; else 0.
+size_t one_range_bytes(const pa_graph_runner& r) {
+  const pa_runner_buffers& b = r.buf;
+  if (!b.new_key) return 0;
+  const char* d0 = static_cast<const char*>(b.q);
+  const char* h0 = static_cast<const char*>(b.h_q);
+  const void* dev[4] = {b.new_key, b.new_value, b.block_tables, b.context_lens};
+  const void* host[4] = {b.h_new_key, b.h_new_value, b.h_block_tables, b.h_context_lens};
+  const char* prev = d0;
+  for (int i = 0; i < 4; ++i) {
+    const char* d = static_cast<const char*>(dev[i]);
+    if (d <= prev || d - d0 != static_cast<const char*>(host[i]) - h0) return 0;
+    prev = d;
+  }
+  const size_t bmax = static_cast<size_t>(r.classes.back());
+  return static_cast<size_t>(reinterpret_cast<const char*>(b.context_lens + bmax) - d0);
+}
+
+// One step of num_seqs sequences as it is captured: [staging copies in],
+// pa_attention, [staging copy out].
+pa_status step_for(const pa_graph_runner& r, int num_seqs, cudaStream_t s) {
   const pa_runner_config& c = r.cfg;
   const pa_runner_buffers& b = r.buf;
-  return pa_attention(b.out, b.q, b.new_key, b.new_value, b.k_cache, b.v_cache, b.k_scale,
-                      b.v_scale, c.kv_dtype, c.window_size, b.block_tables,
-                      c.max_blocks_per_seq, b.context_lens, c.max_context_len, num_seqs,
-                      c.num_query_tokens, c.num_blocks, c.num_q_heads, c.num_kv_heads,
-                      c.head_dim, c.block_size, c.scale, partition_for(c, num_seqs),
-                      b.workspace, b.workspace_bytes, reinterpret_cast<pa_stream_t>(s));
+  const size_t rows = static_cast<size_t>(num_seqs) * c.num_query_tokens;
+  const size_t q_bytes = rows * c.num_q_heads * c.head_dim * 2;
+  const size_t kv_bytes = rows * c.num_kv_heads * c.head_dim * 2;
+  const bool stage = staged(b);
+  const size_t one = stage ? one_range_bytes(r) : 0;
+  if (one > 0) {
+    // every input in one copy (the whole range, sized for the largest class)
+    if (cudaMemcpyAsync(b.q, b.h_q, one, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return PA_ERR_CUDA;
+  } else if (stage) {
+    if (cudaMemcpyAsync(b.q, b.h_q, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        (b.new_key && (cudaMemcpyAsync(b.new_key, b.h_new_key, kv_bytes,
+                                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
+                       cudaMemcpyAsync(b.new_value, b.h_new_value, kv_bytes,
+                                       cudaMemcpyHostToDevice, s) != cudaSuccess)) ||
+        cudaMemcpyAsync(b.block_tables, b.h_block_tables,
+                        static_cast<size_t>(num_seqs) * c.max_blocks_per_seq * 4,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(b.context_lens, b.h_context_lens, static_cast<size_t>(num_seqs) * 4,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  const pa_status st =
+      pa_attention(b.out, b.q, b.new_key, b.new_value, b.k_cache, b.v_cache, b.k_scale,
+                   b.v_scale, c.kv_dtype, c.window_size, b.block_tables, c.max_blocks_per_seq,
+                   b.context_lens, c.max_context_len, num_seqs, c.num_query_tokens,
+                   c.num_blocks, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size,
+                   c.scale, partition_for(c, num_seqs), b.workspace, b.workspace_bytes,
+                   reinterpret_cast<pa_stream_t>(s));
+  if (st != PA_OK) return st;
+  if (stage && cudaMemcpyAsync(b.h_out, b.out, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
 }
 
 }  // namespace
@@ -84,7 +138,7 @@ pa_status pa_runner_create(const pa_runner_config* cfg, const pa_runner_buffers*
       delete r;
       return PA_ERR_CUDA;
     }
-    const pa_status st = attention_for(*r, c, r->capture_stream);
+    const pa_status st = step_for(*r, c, r->capture_stream);
     const cudaError_t ce = cudaStreamEndCapture(r->capture_stream, &graph);
     if (st != PA_OK || ce != cudaSuccess || graph == nullptr) {
       if (graph) cudaGraphDestroy(graph);
@@ -117,11 +171,19 @@ pa_status pa_runner_step(pa_graph_runner* r, int num_seqs, pa_stream_t stream) {
   if (it == r->classes.end()) return PA_ERR_UNSUPPORTED;
   const int c = *it;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (c > num_seqs &&
-      pa::launch_pad_rows(r->buf.block_tables, r->buf.context_lens, num_seqs, c,
-                          r->cfg.max_blocks_per_seq, r->cfg.pad_block,
-                          r->cfg.num_query_tokens, s) != cudaSuccess)
+  if (c > num_seqs && staged(r->buf)) {
+    // pad the host rows; the class graph copies them in with the real ones
+    for (int row = num_seqs; row < c; ++row) {
+      int32_t* t = r->buf.h_block_tables + static_cast<size_t>(row) * r->cfg.max_blocks_per_seq;
+      std::fill(t, t + r->cfg.max_blocks_per_seq, r->cfg.pad_block);
+      r->buf.h_context_lens[row] = r->cfg.num_query_tokens;
+    }
+  } else if (c > num_seqs &&
+             pa::launch_pad_rows(r->buf.block_tables, r->buf.context_lens, num_seqs, c,
+                                 r->cfg.max_blocks_per_seq, r->cfg.pad_block,
+                                 r->cfg.num_query_tokens, s) != cudaSuccess) {
     return PA_ERR_CUDA;
+  }
   return cudaGraphLaunch(r->execs[static_cast<size_t>(it - r->classes.begin())], s) ==
                  cudaSuccess
              ? PA_OK

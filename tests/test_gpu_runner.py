@@ -112,6 +112,33 @@ def test_default_partition_per_class():
     r.close()
 
 
+def test_host_staging_copies_inside_the_graph():
+    """With host staging the class graph copies the host inputs in and the output back:
+    the host output rows equal a direct call, and host padding rows are rewritten."""
+    w = make(T=1, n=16, seed=52)
+    mcl, psize = int(w.context_lens.max()), 256
+    k, v = to_dev(w.k_cache), to_dev(w.v_cache)
+    pad = pad_block_of(w)
+    r = pa.GraphRunner(k, v, w.num_q_heads, mcl, w.max_blocks_per_seq, pad, psize,
+                       classes=(2, 8, 16), scale=w.scale, host_staging=True)
+    for B in (1, 5, 16):
+        q, nk, nv, tb, ln, _ = sub(w, B)
+        r.h_q[:B].copy_(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16))
+        r.h_new_key[:B].copy_(torch.from_numpy(nk.view(np.int16)).view(torch.bfloat16))
+        r.h_new_value[:B].copy_(torch.from_numpy(nv.view(np.int16)).view(torch.bfloat16))
+        r.h_block_tables[:B].copy_(torch.from_numpy(tb))
+        r.h_context_lens[:B].copy_(torch.from_numpy(ln))
+        r.step(B)
+        torch.cuda.synchronize()
+        c = r.class_of(B)
+        assert (r.h_block_tables[B:c] == pad).all() and (r.h_context_lens[B:c] == 1).all()
+        k2, v2 = to_dev(w.k_cache), to_dev(w.v_cache)
+        want = pa.attention(to_dev(q), k2, v2, to_dev(tb), to_dev(ln), mcl, w.scale, psize,
+                            new_key=to_dev(nk), new_value=to_dev(nv))
+        assert torch.equal(r.h_out[:B].view(torch.int16), want.cpu().view(torch.int16)), f"B={B}"
+    r.close()
+
+
 def test_runner_with_window_and_fp8_pages():
     base = make(T=2, n=8, seed=5)
     w = W.fp8_variant(base, seed=2)
