@@ -142,10 +142,11 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   __shared__ int s_nmem;
   __shared__ int s_bad;
 
-  if constexpr (GROUP) {
-    // The per-sequence kernel of the same call may run alongside this one.
-    grid_launch_dependents();
-  } else if (blockIdx.x == gridDim.x - 1) {
+  // The kernel launched next may start once every CTA of this grid has started:
+  // the per-sequence kernel of the same call after the shared-prefix kernel, the
+  // split-KV merge (which waits for this grid's completion) after the per-sequence one.
+  grid_launch_dependents();
+  if (!GROUP && blockIdx.x == gridDim.x - 1) {
     // When launched alongside a shared-prefix kernel, this grid must not
     // complete before it (the split-KV merge that follows reads both).
     grid_dependency_wait();

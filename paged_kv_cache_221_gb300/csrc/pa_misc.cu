@@ -157,10 +157,17 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
 // w_i = l_i 2^(m_i - M), M = max_i m_i.  Warp k of a row merges partitions
 // k, k + W, ... against its own max (lane j weighting partition j of each
 // block of 32, every lane summing its head dims with eight 16-byte loads in
-// flight); the W partial merges are then combined by the same rule.
+// flight); the W partial merges are then combined by the same rule.  A warp
+// with at most kMergeFast partitions issues all their (m, l) and O loads at
+// once, before it knows M, so the merge costs one memory round trip.
 // Sequences that fit in one partition were written by the attention kernel
 // directly and are skipped (same predicate).
+// The kernel is launched as a programmatic dependent of the attention kernel
+// (whose CTAs trigger at their start): it may become resident during the
+// attention kernel's last wave and waits for that grid's completion before it
+// reads any partial.
 constexpr int kMergeWarps = 4;
+constexpr int kMergeFast = 12;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32)
@@ -198,12 +205,49 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   // this warp's partitions: sub, sub + W, sub + 2W, ...
   const int mine = live ? (nparts - sub + W - 1) / W : 0;
   float M = -CUDART_INF_F;
-  for (int k = lane; k < mine; k += 32) M = fmaxf(M, ml[sub + k * W].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float S = 0.f, acc[DL];
 #pragma unroll
   for (int k = 0; k < DL; ++k) acc[k] = 0.f;
+  grid_dependency_wait();                    // the attention grid's partials are complete
+  if (mine <= kMergeFast) {
+    // every lane loads every (m, l) (one broadcast each) and its head dims of every O
+    float2 mv[kMergeFast];
+    float xv[kMergeFast][DL];
+#pragma unroll
+    for (int k = 0; k < kMergeFast; ++k) {
+      mv[k] = make_float2(-CUDART_INF_F, 0.f);
+#pragma unroll
+      for (int d = 0; d < DL; ++d) xv[k][d] = 0.f;
+      if (k < mine) {
+        mv[k] = ml[sub + k * W];
+        const float* src = po + static_cast<size_t>(sub + k * W) * D;
+        if constexpr (DL == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src);
+          xv[k][0] = x.x;
+          xv[k][1] = x.y;
+          xv[k][2] = x.z;
+          xv[k][3] = x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(src);
+          xv[k][0] = x.x;
+          xv[k][1] = x.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kMergeFast; ++k) M = fmaxf(M, mv[k].x);
+#pragma unroll
+    for (int k = 0; k < kMergeFast; ++k) {
+      const float w = (mv[k].x == -CUDART_INF_F || M == -CUDART_INF_F)
+                          ? 0.f : mv[k].y * exp2f(mv[k].x - M);
+      S += w;
+#pragma unroll
+      for (int d = 0; d < DL; ++d) acc[d] += w * xv[k][d];
+    }
+  } else {
+  for (int k = lane; k < mine; k += 32) M = fmaxf(M, ml[sub + k * W].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   for (int base = 0; base < mine; base += 32) {
     // (m, l) of this lane's partition of the block (an L1 hit, loaded just above)
     const float2 mlv = base + lane < mine ? ml[sub + (base + lane) * W]
@@ -231,6 +275,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  }
 
   if (W > 1) {
     // combine the W partial merges of the row: weights 2^(M_k - M_row)
@@ -269,11 +314,18 @@ cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s) {
   const long long chunks = (static_cast<long long>(p.G) * p.T + rows_per_cta - 1) / rows_per_cta;
   const long long ctas = static_cast<long long>(p.num_seqs) * p.Hkv * chunks;
   if (ctas == 0) return cudaSuccess;
-  if (head_dim == 64)
-    splitkv_reduce_kernel<64><<<static_cast<unsigned>(ctas), kMergeWarps * 32, 0, s>>>(p, W);
-  else
-    splitkv_reduce_kernel<128><<<static_cast<unsigned>(ctas), kMergeWarps * 32, 0, s>>>(p, W);
-  return cudaGetLastError();
+  // programmatic stream serialisation: may start during the attention kernel's last wave
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (head_dim == 64) return cudaLaunchKernelEx(&cfg, splitkv_reduce_kernel<64>, p, W);
+  return cudaLaunchKernelEx(&cfg, splitkv_reduce_kernel<128>, p, W);
 }
 
 // ---------------------------------------------------------------- graph runner padding
