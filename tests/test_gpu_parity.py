@@ -58,6 +58,24 @@ def test_partition_sizes(name, psize):
     assert_close(d.attend(partition_size=psize), ref, what=f"{name} psize {psize}")
 
 
+@pytest.mark.parametrize("lens", [[368, 384, 400, 411, 496], [767, 768, 784, 785, 960]])
+def test_merge_partition_counts(lens):
+    """Split-KV merge at the boundary of its two load schedules.  With one-block
+    partitions, at most 31 partitions (first case) give 2 merging warps per row and
+    more give 4 (second case); a warp holding up to 12 partitions issues all their
+    loads at once, one holding 13 or more loops over them (23/24 partitions: 12 per
+    warp; 25/26: 13; 48: 12 per warp of 4; 49/50: 13 on the first)."""
+    w = W.build("merge_edge", lens, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                seed=sum(lens) % 997)
+    ref, _, _ = O.run_workload(w)
+    d = Dev(w)
+    d.reshape()
+    assert_close(d.attend(partition_size=16), ref, what=f"merge {lens}")
+    # the same rows through the fused append call
+    d2 = Dev(w)
+    assert_close(d2.attend_append(partition_size=16), ref, what=f"merge append {lens}")
+
+
 def test_unsplit_without_workspace():
     """partition_size 0 and no workspace: every sequence in one CTA per kv head."""
     w = W.SMALL["decode_8b"]()
