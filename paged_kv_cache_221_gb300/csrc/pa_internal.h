@@ -91,6 +91,9 @@ cudaError_t launch_spec_accept(const float* p, const float* q, const int32_t* dr
 // in block `pad_block`.
 cudaError_t launch_pad_rows(int32_t* block_tables, int32_t* context_lens, int from, int to,
                             int max_blocks_per_seq, int pad_block, int len, cudaStream_t s);
+// Graph runner staging: `bytes` (a multiple of 16; both addresses 16-byte aligned and
+// device-addressable) copied by a kernel.
+cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t s);
 cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, void* v_cache,
                            const int64_t* slots, int num_tokens, int num_blocks, int hkv,

@@ -328,6 +328,27 @@ cudaError_t launch_reduce(const AttnParams& p, int head_dim, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, splitkv_reduce_kernel<128>, p, W);
 }
 
+// ---------------------------------------------------------------- graph runner staging
+// Copy of 16-byte vectors by the SMs.  Used by the graph runner to move a step's
+// inputs from page-locked host memory and its output back: host memory that the
+// device addresses directly (unified addressing over the CPU-GPU link), so a
+// small copy costs one kernel instead of a copy-engine transfer.
+__global__ void stage_copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                  long long n) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
+cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return cudaSuccess;
+  const long long n = static_cast<long long>(bytes / 16);
+  const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 2 * 152));
+  stage_copy_kernel<<<blocks, 256, 0, s>>>(static_cast<uint4*>(dst),
+                                           static_cast<const uint4*>(src), n);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- graph runner padding
 __global__ void pad_rows_kernel(int32_t* __restrict__ tables, int32_t* __restrict__ lens,
                                 int from, int to, int mbs, int pad_block, int len) {

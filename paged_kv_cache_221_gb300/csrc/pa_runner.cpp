@@ -22,6 +22,7 @@
 struct pa_graph_runner {
   pa_runner_config cfg{};
   pa_runner_buffers buf{};
+  bool kernel_copy = false;                  // staging copies by the SMs (see stage_copy)
   std::vector<int> classes;
   std::vector<cudaGraphExec_t> execs;
   cudaStream_t capture_stream = nullptr;
@@ -46,6 +47,28 @@ int partition_for(const pa_runner_config& c, int num_seqs) {
 bool staged(const pa_runner_buffers& b) {
   return b.h_q && b.h_block_tables && b.h_context_lens && b.h_out &&
          (b.new_key == nullptr || (b.h_new_key && b.h_new_value));
+}
+
+// Page-locked host memory that the device addresses with the same pointer
+// (unified addressing): the staging copies can then run as a kernel.
+bool device_addressable_host(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();                      // clear the error of an unknown pointer
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// One staging copy: by the SMs when both sides are device-addressable and 16-byte
+// aligned (one kernel, no copy-engine transfer setup), else by cudaMemcpyAsync.
+cudaError_t stage_copy(const pa_graph_runner& r, void* dst, const void* src, size_t bytes,
+                       cudaMemcpyKind kind, cudaStream_t s) {
+  if (r.kernel_copy && bytes % 16 == 0 && aligned16(dst) && aligned16(src))
+    return pa::launch_stage_copy(dst, src, bytes, s);
+  return cudaMemcpyAsync(dst, src, bytes, kind, s);
 }
 
 // When the host inputs and the device inputs each form one range, in the same
@@ -78,21 +101,20 @@ pa_status step_for(const pa_graph_runner& r, int num_seqs, cudaStream_t s) {
   const size_t kv_bytes = rows * c.num_kv_heads * c.head_dim * 2;
   const bool stage = staged(b);
   const size_t one = stage ? one_range_bytes(r) : 0;
+  constexpr cudaMemcpyKind H2D = cudaMemcpyHostToDevice;
   if (one > 0) {
     // every input in one copy (the whole range, sized for the largest class)
-    if (cudaMemcpyAsync(b.q, b.h_q, one, cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return PA_ERR_CUDA;
+    if (stage_copy(r, b.q, b.h_q, one, H2D, s) != cudaSuccess) return PA_ERR_CUDA;
   } else if (stage) {
-    if (cudaMemcpyAsync(b.q, b.h_q, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        (b.new_key && (cudaMemcpyAsync(b.new_key, b.h_new_key, kv_bytes,
-                                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
-                       cudaMemcpyAsync(b.new_value, b.h_new_value, kv_bytes,
-                                       cudaMemcpyHostToDevice, s) != cudaSuccess)) ||
-        cudaMemcpyAsync(b.block_tables, b.h_block_tables,
-                        static_cast<size_t>(num_seqs) * c.max_blocks_per_seq * 4,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(b.context_lens, b.h_context_lens, static_cast<size_t>(num_seqs) * 4,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+    if (stage_copy(r, b.q, b.h_q, q_bytes, H2D, s) != cudaSuccess ||
+        (b.new_key && (stage_copy(r, b.new_key, b.h_new_key, kv_bytes, H2D, s) != cudaSuccess ||
+                       stage_copy(r, b.new_value, b.h_new_value, kv_bytes, H2D, s) !=
+                           cudaSuccess)) ||
+        stage_copy(r, b.block_tables, b.h_block_tables,
+                   static_cast<size_t>(num_seqs) * c.max_blocks_per_seq * 4, H2D, s) !=
+            cudaSuccess ||
+        stage_copy(r, b.context_lens, b.h_context_lens, static_cast<size_t>(num_seqs) * 4, H2D,
+                   s) != cudaSuccess)
       return PA_ERR_CUDA;
   }
   const pa_status st =
@@ -103,7 +125,7 @@ pa_status step_for(const pa_graph_runner& r, int num_seqs, cudaStream_t s) {
                    c.scale, partition_for(c, num_seqs), b.workspace, b.workspace_bytes,
                    reinterpret_cast<pa_stream_t>(s));
   if (st != PA_OK) return st;
-  if (stage && cudaMemcpyAsync(b.h_out, b.out, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (stage && stage_copy(r, b.h_out, b.out, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }
@@ -128,6 +150,14 @@ pa_status pa_runner_create(const pa_runner_config* cfg, const pa_runner_buffers*
   r->buf = *buffers;
   r->classes.assign(cfg->classes, cfg->classes + cfg->num_classes);
   r->cfg.classes = nullptr;                   // the runner keeps its own copy
+  if (staged(r->buf)) {
+    const pa_runner_buffers& b = r->buf;
+    r->kernel_copy = device_addressable_host(b.h_q) && device_addressable_host(b.h_block_tables) &&
+                     device_addressable_host(b.h_context_lens) &&
+                     device_addressable_host(b.h_out) &&
+                     (b.new_key == nullptr || (device_addressable_host(b.h_new_key) &&
+                                               device_addressable_host(b.h_new_value)));
+  }
   if (cudaStreamCreateWithFlags(&r->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
     delete r;
     return PA_ERR_CUDA;
