@@ -476,9 +476,12 @@ typedef struct pa_runner_buffers {   /* device pointers, as for pa_attention */
    * instead of launching the padding kernel.  When the five host inputs and the
    * five device inputs each lie in one range, in the order q, new_key,
    * new_value, block_tables, context_lens and at the same offsets, the graph
-   * copies that whole range (sized for the largest class) in one piece.  Read
-   * h_out, and rewrite the host
-   * inputs for the next step, only after the stream has finished the step. */
+   * copies that whole range (sized for the largest class) in one piece.  When
+   * every host buffer is page-locked memory that the device addresses with the
+   * same pointer (checked once, at creation), the copies are made by a kernel
+   * of the class graph (16-byte vectors; sizes and addresses multiples of 16),
+   * otherwise by cudaMemcpyAsync.  Read h_out, and rewrite the host inputs for
+   * the next step, only after the stream has finished the step. */
   void* h_q;
   void* h_new_key;
   void* h_new_value;
