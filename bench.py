@@ -556,7 +556,8 @@ def run_gb300(args):
         "kv_bytes_per_step": kv_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(w.name),
+                     # the recorded captures are of full-context launches
+                     "traffic": recorded_traffic(w.name) if args.window <= 0 else None,
                      "kernel": "attention call (paged_attn_kernel + splitkv_reduce_kernel)",
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "launch_ms_avg": round(attn_avg, 5)},
