@@ -245,36 +245,36 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
       for (int d = 0; d < DL; ++d) acc[d] += w * xv[k][d];
     }
   } else {
-  for (int k = lane; k < mine; k += 32) M = fmaxf(M, ml[sub + k * W].x);
+    for (int k = lane; k < mine; k += 32) M = fmaxf(M, ml[sub + k * W].x);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  for (int base = 0; base < mine; base += 32) {
-    // (m, l) of this lane's partition of the block (an L1 hit, loaded just above)
-    const float2 mlv = base + lane < mine ? ml[sub + (base + lane) * W]
-                                          : make_float2(-CUDART_INF_F, 0.f);
-    const float w = (mlv.x == -CUDART_INF_F || M == -CUDART_INF_F) ? 0.f
-                                                                  : mlv.y * exp2f(mlv.x - M);
-    S += w;
-    const int n = min(32, mine - base);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int base = 0; base < mine; base += 32) {
+      // (m, l) of this lane's partition of the block (an L1 hit, loaded just above)
+      const float2 mlv = base + lane < mine ? ml[sub + (base + lane) * W]
+                                            : make_float2(-CUDART_INF_F, 0.f);
+      const float w = (mlv.x == -CUDART_INF_F || M == -CUDART_INF_F) ? 0.f
+                                                                    : mlv.y * exp2f(mlv.x - M);
+      S += w;
+      const int n = min(32, mine - base);
 #pragma unroll 8
-    for (int k = 0; k < n; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      const float* src = po + static_cast<size_t>(sub + (base + k) * W) * D;
-      if constexpr (DL == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] += wk * x.x;
-        acc[1] += wk * x.y;
-        acc[2] += wk * x.z;
-        acc[3] += wk * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] += wk * x.x;
-        acc[1] += wk * x.y;
+      for (int k = 0; k < n; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        const float* src = po + static_cast<size_t>(sub + (base + k) * W) * D;
+        if constexpr (DL == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src);
+          acc[0] += wk * x.x;
+          acc[1] += wk * x.y;
+          acc[2] += wk * x.z;
+          acc[3] += wk * x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(src);
+          acc[0] += wk * x.x;
+          acc[1] += wk * x.y;
+        }
       }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
   }
 
   if (W > 1) {
