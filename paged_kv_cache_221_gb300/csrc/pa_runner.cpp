@@ -103,8 +103,12 @@ pa_status step_for(const pa_graph_runner& r, int num_seqs, cudaStream_t s) {
   const size_t one = stage ? one_range_bytes(r) : 0;
   constexpr cudaMemcpyKind H2D = cudaMemcpyHostToDevice;
   if (one > 0) {
-    // every input in one copy (the whole range, sized for the largest class)
-    if (stage_copy(r, b.q, b.h_q, one, H2D, s) != cudaSuccess) return PA_ERR_CUDA;
+    // every input in one copy (the whole range, sized for the largest class); a
+    // kernel reads it only if its last byte is device-addressable host memory too
+    const bool end_ok = device_addressable_host(static_cast<const char*>(b.h_q) + one - 1);
+    if ((end_ok ? stage_copy(r, b.q, b.h_q, one, H2D, s)
+                : cudaMemcpyAsync(b.q, b.h_q, one, H2D, s)) != cudaSuccess)
+      return PA_ERR_CUDA;
   } else if (stage) {
     if (stage_copy(r, b.q, b.h_q, q_bytes, H2D, s) != cudaSuccess ||
         (b.new_key && (stage_copy(r, b.new_key, b.h_new_key, kv_bytes, H2D, s) != cudaSuccess ||
