@@ -30,6 +30,7 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "paged decode-attention KV-read GB/s vs GB300 HBM peak; seq-steps/sec"
+L2_BYTES = 129 * 1000 * 1000     # GB300 L2
 KERNEL_SOURCES = ["pa_attn.cuh", "pa_ptx.cuh"]   # the attention kernel template and its PTX
 KERNEL_PARAMS = "pa_internal.h"                  # its constants and AttnParams (up to the struct end)
 WORKLOAD_DESC = {
@@ -217,8 +218,10 @@ def workload_config(w, ps, world, window=0):
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": w.block_size, "pool_blocks": w.num_blocks,
             "partition_size": ps, "global_batch": w.num_seqs * world, "window": window,
-            "l2": "inputs larger than L2: each step reads %.2f GB of a %.2f GB pool (L2 129 MB)"
-                  % (w.kv_bytes() / 1e9, pool / 1e9),
+            "l2": (("inputs larger than L2: each step reads %.2f GB of a %.2f GB pool "
+                    "(L2 129 MB)") % (w.kv_bytes() / 1e9, pool / 1e9)) if pool > L2_BYTES else
+                  (("inputs smaller than L2 (%.2f MB pool): L2-resident and launch-bound, "
+                    "not a bandwidth figure") % (pool / 1e6)),
             "parallelism": "replicas" if world == 1 else f"replicas x{world}"}
 
 
