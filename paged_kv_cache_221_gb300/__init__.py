@@ -36,6 +36,7 @@ from ._lib import PagedAttnError, STATUS_NAMES
 __all__ = ["reshape_and_cache", "decode", "verify", "decode_shared_prefix", "workspace_size",
            "default_partition_size", "get_device_error", "selftest_wait_timeout", "library",
            "copy_blocks", "BlockManager", "reshape_and_cache_fp8", "decode_fp8", "verify_fp8",
+           "attention", "spec_accept", "GraphRunner",
            "PagedAttnError", "STATUS_NAMES"]
 
 
