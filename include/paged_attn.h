@@ -344,19 +344,29 @@ pa_status pa_decode_shared_prefix_fp8(
  * paper has no counterpart; this is a library convenience.
  *
  * The split-KV scratch comes from one fixed array of 32 MiB (33554432 bytes)
- * inside this library's device image.  It exists on every GPU the library is
- * loaded on and is held until the process exits.  If the call needs more than
- * 32 MiB (the scratch pa_decode needs with these sizes, num_kv_heads included)
- * it returns PA_ERR_WORKSPACE and launches nothing.
- * Nothing is allocated by this call or by anything it calls.
+ * inside this library's device image, held until the process exits on every
+ * GPU where it has been loaded.  If the call needs more than 32 MiB (the
+ * scratch pa_decode needs with these sizes, num_kv_heads included): with
+ * partition_size 0 it attends over whole sequences, which needs no scratch
+ * (the result pa_decode gives without a workspace); with an explicit
+ * partition_size it returns PA_ERR_WORKSPACE and launches nothing.  Argument
+ * errors take precedence over PA_ERR_WORKSPACE, as in pa_decode.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls in the process share the one array
- * and it keeps what the last call wrote; nothing in it needs to start at zero
- * (every partial is written before it is read).  Calls whose executions
- * overlap on the GPU (e.g. on two streams) race on the array: serialise them.
- * Arguments, results and errors are otherwise those of pa_decode.
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress).  Under CUDA's lazy module
+ * loading, the default, that lookup is also what loads the array onto the
+ * device, so that first call reserves the 32 MiB (with
+ * CUDA_MODULE_LOADING=EAGER the array is loaded with the library instead).
+ * Make the first call on each device during start-up, before the rest of
+ * device memory is reserved and before any stream capture.  A failed lookup
+ * returns PA_ERR_CUDA (when the call needs scratch) and is retried by the next
+ * call.  After set-up, no call allocates device memory.
+ *
+ * All calls in the process share the one array and it keeps what the last
+ * call wrote; nothing in it needs to start at zero (every partial is written
+ * before it is read).  Calls whose executions overlap on the GPU (e.g. on two
+ * streams) race on the array: serialise them.  Arguments, results and errors
+ * are otherwise those of pa_decode.
  */
 pa_status pa_decode_static_scratch(void* out, const void* q, const void* k_cache,
                                    const void* v_cache, const int32_t* block_tables,

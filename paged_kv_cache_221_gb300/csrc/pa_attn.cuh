@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <atomic>
 #include <climits>
 #include <type_traits>
 
@@ -836,14 +837,19 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const AttnP
                        dim3 grid, cudaStream_t s, bool overlap_previous) {
   constexpr int smem = Smem<D, C::NT, C::NTW, KV8>::kAlloc;
   auto kern = paged_attn_kernel<D, C, GROUP, KV8>;
-  static int configured_device = -1;         // attribute set once per device in practice
+  // The shared-memory attribute is per device: one bit per device (ids below 64)
+  // records that it has been set.  Host threads driving different devices may
+  // race here; setting the attribute twice is harmless, and a failed attempt
+  // records nothing, so the next call tries again.
+  static std::atomic<unsigned long long> configured{0ull};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit == 0 || (configured.load(std::memory_order_acquire) & bit) == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   if (!overlap_previous) {
     kern<<<grid, C::kThreads, smem, s>>>(tk, tv, p);

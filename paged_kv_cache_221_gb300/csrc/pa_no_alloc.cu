@@ -7,10 +7,12 @@
 // cudaFree afterwards (both can synchronise the device and fragment the
 // memory that was planned for the KV cache).  Such a caller cannot provide the
 // split-KV scratch that pa_decode needs for long contexts.  This entry point
-// takes that scratch from a fixed array that lives in this library's device
-// image instead: the array is created when the library's module is loaded on a
-// device and stays there until the process exits, on every GPU the library
-// is loaded on.
+// takes that scratch from a fixed array in this library's device image
+// instead.  The array belongs to this file's module: under CUDA's lazy module
+// loading (the default) the module, and with it the array's 32 MiB, is loaded
+// onto a device by the first call made on that device, which looks up the
+// array's address; with CUDA_MODULE_LOADING=EAGER it is loaded with the
+// library.  Either way it stays until the process exits.
 #include <mutex>
 
 #include "paged_attn.h"
@@ -24,23 +26,28 @@ constexpr size_t kStaticScratchBytes = 32ull << 20;   // 32 MiB
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
-cudaError_t g_scratch_status[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mutex[kMaxDevices];
+void* g_scratch_addr[kMaxDevices];            // set once the lookup has succeeded
 
-// Device address of the array on the current device, looked up once per device.
-// (On the host, `g_decode_scratch` names a host-side stand-in, not device memory.)
+// Device address of the array on the current device.  A successful lookup is
+// kept; a failed one (for instance no memory left to load the module) is not,
+// so the next call tries again.  (On the host, `g_decode_scratch` names a
+// host-side stand-in, not device memory.)
 cudaError_t scratch_address(void** addr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_scratch_mutex[dev]);
+  if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    g_scratch_status[dev] = cudaGetSymbolAddress(&p, g_decode_scratch);
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) {
+      cudaGetLastError();                       // do not leave the error for the next launch
+      return e;
+    }
     g_scratch_addr[dev] = p;
-  });
-  if (g_scratch_status[dev] != cudaSuccess) return g_scratch_status[dev];
+  }
   *addr = g_scratch_addr[dev];
   return cudaSuccess;
 }
@@ -57,13 +64,26 @@ extern "C" pa_status pa_decode_static_scratch(
     return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                      max_context_len, num_seqs, num_blocks, num_q_heads, num_kv_heads,
                      head_dim, block_size, scale, partition_size, nullptr, 0, stream);
+  // Set-up on the first call on this device, whether or not this call needs scratch.
+  void* ws = nullptr;
+  const cudaError_t se = scratch_address(&ws);
   const size_t need = pa::workspace_for(num_seqs, num_q_heads, num_kv_heads, 1,
                                         max_context_len, head_dim, partition_size, 0);
-  if (need > kStaticScratchBytes) return PA_ERR_WORKSPACE;
-  void* ws = nullptr;
-  if (need > 0 && scratch_address(&ws) != cudaSuccess) return PA_ERR_CUDA;
+  if (need == 0)
+    return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                     max_context_len, num_seqs, num_blocks, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, partition_size, nullptr, 0, stream);
+  if (need > kStaticScratchBytes) {
+    // Without scratch pa_decode runs its own checks first.  With the default
+    // partition size (0) it then attends over whole sequences, which needs no
+    // scratch; with an explicit partition size it returns PA_ERR_WORKSPACE
+    // before launching anything.
+    return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                     max_context_len, num_seqs, num_blocks, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, partition_size, nullptr, 0, stream);
+  }
+  if (se != cudaSuccess) return PA_ERR_CUDA;
   return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                    max_context_len, num_seqs, num_blocks, num_q_heads, num_kv_heads, head_dim,
-                   block_size, scale, partition_size, ws, need > 0 ? kStaticScratchBytes : 0,
-                   stream);
+                   block_size, scale, partition_size, ws, kStaticScratchBytes, stream);
 }
