@@ -136,6 +136,93 @@ def test_planted_mistake_no_copy_on_write_is_caught():
         OBM.BlockManager = orig
 
 
+# ----------------------------------------------------------------------------- block copy
+
+def _copy_case(seed=5, nb=12, hkv=3, d=8):
+    """Pools whose every element is distinct, and copy pairs (no destination is a source)."""
+    rng = np.random.default_rng(seed)
+    vals = rng.permutation(2 * nb * hkv * BS * d).astype(np.uint16)
+    k = vals[:nb * hkv * BS * d].reshape(nb, hkv, BS, d)
+    v = vals[nb * hkv * BS * d:].reshape(nb, hkv, BS, d)
+    pairs = [(0, 7), (3, 4), (3, 9), (11, 2)]
+    return k, v, pairs
+
+
+def pin_copy_blocks_scalar(cb):
+    """Every element of each destination block, both pools, equals the source's, read by
+    scalar loops; every other block is unchanged, and the inputs are not modified."""
+    k, v, pairs = _copy_case()
+    k0, v0 = k.copy(), v.copy()
+    kk, vv = cb(k, v, pairs)
+    np.testing.assert_array_equal(k, k0)
+    np.testing.assert_array_equal(v, v0)
+    nb, hkv, bs, d = k.shape
+    dst = {b for _, b in pairs}
+    for src, b in pairs:
+        for h in range(hkv):
+            for o in range(bs):
+                for x in range(d):
+                    assert kk[b, h, o, x] == k0[src, h, o, x]
+                    assert vv[b, h, o, x] == v0[src, h, o, x]
+    for b in range(nb):
+        if b not in dst:
+            assert (kk[b] == k0[b]).all() and (vv[b] == v0[b]).all()
+
+
+def pin_copy_blocks_empty(cb):
+    k, v, _ = _copy_case(seed=6)
+    kk, vv = cb(k, v, [])
+    np.testing.assert_array_equal(kk, k)
+    np.testing.assert_array_equal(vv, v)
+
+
+COPY_PINS = [pin_copy_blocks_scalar, pin_copy_blocks_empty]
+
+
+@pytest.mark.parametrize("pin", COPY_PINS, ids=[p.__name__ for p in COPY_PINS])
+def test_copy_pin(pin):
+    pin(OBM.copy_blocks)
+
+
+def _copy_swapped(k_cache, v_cache, pairs):
+    return OBM.copy_blocks(k_cache, v_cache, [(d, s) for s, d in pairs])
+
+
+def _copy_k_only(k_cache, v_cache, pairs):
+    k, _ = OBM.copy_blocks(k_cache, v_cache, pairs)
+    return k, np.array(v_cache, copy=True)
+
+
+def _copy_in_place(k_cache, v_cache, pairs):
+    for s, d in pairs:
+        k_cache[d] = k_cache[s]
+        v_cache[d] = v_cache[s]
+    return k_cache, v_cache
+
+
+def _copy_first_head(k_cache, v_cache, pairs):
+    k, v = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+    for s, d in pairs:
+        k[d, 0] = k_cache[s, 0]
+        v[d, 0] = v_cache[s, 0]
+    return k, v
+
+
+COPY_MUTANTS = {"src_dst_swapped": _copy_swapped, "k_pool_only": _copy_k_only,
+                "inputs_modified": _copy_in_place, "first_head_only": _copy_first_head}
+
+
+@pytest.mark.parametrize("name", sorted(COPY_MUTANTS))
+def test_copy_planted_mistake_is_caught(name):
+    failed = []
+    for pin in COPY_PINS:
+        try:
+            pin(COPY_MUTANTS[name])
+        except Exception:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
+
+
 @pytest.fixture(scope="module")
 def lib():
     __graft_entry__.build()

@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import workloads as W
+from fp8_cases import exact_fp8_case
 from oracle import fp8 as F
 from oracle import oracle as O
 
@@ -150,9 +151,30 @@ def pin_attention_reduces_to_bf16(f):
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
 
 
+def pin_run_workload_reduces_to_bf16(f):
+    """The whole FP8 step (quantised append of the new tokens, then attention) on a
+    workload whose every value is exact equals the pinned bf16 oracle's step on the
+    bf16 twin: outputs to 1e-12, and the appended slots hold exactly the twin's values
+    (K and V scales differ, so mixing them up fails)."""
+    w, twin = exact_fp8_case()
+    got, k, v = f.run_workload(w)
+    want, kb, vb = O.run_workload(twin)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+    blk, off = np.divmod(w.slot_mapping, w.block_size)
+    kval = torch_decode(k[blk, :, off, :]) * w.k_scale[None, :, None]
+    vval = torch_decode(v[blk, :, :, off]) * w.v_scale[None, :, None]
+    np.testing.assert_array_equal(kval, O.bf16_bits_to_f64(kb[blk, :, off, :]))
+    np.testing.assert_array_equal(vval, O.bf16_bits_to_f64(vb[blk, :, off, :]))
+    # only the named sequences are computed; the others stay NaN
+    sub = f.run_workload(w, seqs=[1, 3])[0]
+    np.testing.assert_array_equal(sub[[1, 3]], got[[1, 3]])
+    assert np.isnan(sub[[0, 2]]).all()
+
+
 PINS = [pin_decode_matches_torch, pin_encode_matches_torch, pin_encode_saturates_and_nan,
         pin_round_trip, pin_quantize_divides_in_float32, pin_reshape_layout,
-        pin_attention_reduces_to_bf16]
+        pin_attention_reduces_to_bf16, pin_run_workload_reduces_to_bf16]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -243,7 +265,30 @@ def _gather_v_twice_scaled(v_codes, row, L, g, v_scale, bs):
     return 2.0 * F.gather_v(v_codes, row, L, g, v_scale, bs)
 
 
+def _run_scales_swapped(w, seqs=None):
+    k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
+                               w.v_scale, w.k_scale, w.block_size)
+    return F.paged_attention(w.q, k, v, w.v_scale, w.k_scale, w.block_tables, w.context_lens,
+                             w.scale, w.num_kv_heads, w.block_size, seqs=seqs), k, v
+
+
+def _run_no_append(w, seqs=None):
+    k, v = w.k_codes, w.v_codes
+    return F.paged_attention(w.q, k, v, w.k_scale, w.v_scale, w.block_tables, w.context_lens,
+                             w.scale, w.num_kv_heads, w.block_size, seqs=seqs), k, v
+
+
+def _run_append_scales_swapped(w, seqs=None):
+    k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
+                               w.v_scale, w.k_scale, w.block_size)
+    return F.paged_attention(w.q, k, v, w.k_scale, w.v_scale, w.block_tables, w.context_lens,
+                             w.scale, w.num_kv_heads, w.block_size, seqs=seqs), k, v
+
+
 MUTANTS = {
+    "run_workload_scales_swapped": dict(run_workload=_run_scales_swapped),
+    "run_workload_no_append": dict(run_workload=_run_no_append),
+    "run_workload_append_scales_swapped": dict(run_workload=_run_append_scales_swapped),
     "exponent_bias_8": dict(DECODE_TABLE=_table(_bias8)),
     "subnormal_as_normal": dict(DECODE_TABLE=_table(_subnormal_as_normal)),
     "ties_away_from_zero": dict(encode=_encode_ties_away),

@@ -14,6 +14,8 @@ import numpy as np
 import pytest
 
 import workloads as W
+from fp8_cases import exact_fp8_case
+from oracle import fp8 as F
 from oracle import oracle as O
 from oracle import window as WIN
 
@@ -112,9 +114,42 @@ def pin_brute_force(win):
                     assert abs(o - got[b, t, h, d]) < 1e-12
 
 
+def pin_run_workload_long_window_is_plain_step(win):
+    """The whole windowed step (append, then attention) with a window covering every
+    context equals the pinned plain step, bit for bit, for both page formats."""
+    w = case(T=3)
+    got, k, v = win.run_workload(w, int(w.context_lens.max()))
+    want, kw, vw = O.run_workload(w)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(k, kw)
+    np.testing.assert_array_equal(v, vw)
+    w8, _ = exact_fp8_case(seed=23, lens=(9, 33, 48), T=3)
+    got, k, v = win.run_workload(w8, int(w8.context_lens.max()))
+    want, kw, vw = F.run_workload(w8)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(k, kw)
+    np.testing.assert_array_equal(v, vw)
+
+
+def pin_run_workload_window_of_one_is_new_value(win):
+    """A window of one position: every query token returns the V it appended itself,
+    for both page formats (the FP8 case's new values are exact E4M3 values)."""
+    w = case(T=2)
+    w8, _ = exact_fp8_case(seed=29, lens=(6, 31, 50), T=2)
+    for wk in (w, w8):
+        got = win.run_workload(wk, 1)[0]
+        G = wk.num_q_heads // wk.num_kv_heads
+        for b in range(wk.num_seqs):
+            for t in range(2):
+                for h in range(wk.num_q_heads):
+                    want = O.bf16_bits_to_f64(wk.new_value[b * 2 + t, h // G])
+                    np.testing.assert_array_equal(got[b, t, h], want)
+
+
 PINS = [pin_long_window_is_plain_attention, pin_window_of_one_is_own_value,
         pin_window_equals_truncated_table, pin_verify_rows_are_stacked_windowed_decodes,
-        pin_brute_force]
+        pin_brute_force, pin_run_workload_long_window_is_plain_step,
+        pin_run_workload_window_of_one_is_new_value]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -137,7 +172,31 @@ class Mutant:
         return f
 
 
+def _run_window_plus_one(w, window, seqs=None):
+    return WIN.run_workload(w, window + 1, seqs)
+
+
+def _run_fp8_as_bf16(w, window, seqs=None):
+    k, v = O.reshape_and_cache(w.new_key, w.new_value, w.k_cache, w.v_cache, w.slot_mapping,
+                               w.block_size)
+    return WIN.paged_attention(w.q, k, v, w.block_tables, w.context_lens, w.scale,
+                               w.num_kv_heads, w.block_size, window, seqs), k, v
+
+
+def _run_fp8_scales_swapped(w, window, seqs=None):
+    if w.kv_dtype != "fp8":
+        return WIN.run_workload(w, window, seqs)
+    k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
+                               w.k_scale, w.v_scale, w.block_size)
+    return WIN.paged_attention(w.q, k, v, w.block_tables, w.context_lens, w.scale,
+                               w.num_kv_heads, w.block_size, window, seqs, w.v_scale,
+                               w.k_scale), k, v
+
+
 MUTANTS = {
+    "run_workload_window_plus_one": dict(run_workload=_run_window_plus_one),
+    "run_workload_fp8_as_bf16": dict(run_workload=_run_fp8_as_bf16),
+    "run_workload_fp8_scales_swapped": dict(run_workload=_run_fp8_scales_swapped),
     "window_one_too_long": dict(visible_range=lambda L, T, t, w: (max(0, L - T + t - w), L - T + t)),
     "window_from_context_end": dict(visible_range=lambda L, T, t, w: (max(0, L - w), L - T + t)),
     "window_not_clamped": dict(visible_range=lambda L, T, t, w: (L - T + t - w + 1, L - T + t)),
