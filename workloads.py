@@ -37,8 +37,10 @@ Conventions used by every workload:
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 from typing import Optional
 
 import numpy as np
@@ -47,7 +49,8 @@ NAN_BITS = np.uint16(0x7FC0)   # a quiet-NaN bf16 pattern used as the "never rea
 NAN_E4M3 = np.uint8(0x7F)       # the E4M3 NaN code, the same sentinel for FP8 pages
 BLOCK_SIZE = 16                 # tokens per physical block (the pages' example value)
 
-# Chunk size for random generation (elements); keeps temporaries near 256 MB.
+# Chunk size for random generation (elements): each chunk has its own seeded generator
+# and temporaries of a few hundred MB; chunks run on a thread pool.
 _CHUNK = 1 << 25
 
 
@@ -61,14 +64,34 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((u + bias) >> np.uint32(16)).astype(np.uint16)
 
 
+def _chunked(rng: np.random.Generator, n: int, dtype, fill) -> np.ndarray:
+    """n values made chunk by chunk by ``fill(chunk_rng, count)``.  Each chunk has its
+    own generator seeded from ``rng`` (so the result depends only on ``rng``'s state,
+    not on scheduling), and chunks are filled on a thread pool (NumPy's generators
+    and ufuncs release the GIL on large arrays)."""
+    out = np.empty(n, dtype=dtype)
+    starts = list(range(0, n, _CHUNK))
+    seeds = rng.integers(0, 1 << 63, size=len(starts), dtype=np.int64)
+
+    def one(i):
+        s = starts[i]
+        e = min(n, s + _CHUNK)
+        out[s:e] = fill(np.random.default_rng(int(seeds[i])), e - s)
+
+    if len(starts) <= 1:
+        for i in range(len(starts)):
+            one(i)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(min(len(starts), os.cpu_count() or 4)) as ex:
+            list(ex.map(one, range(len(starts))))
+    return out
+
+
 def normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
     """N(0,1) float32 draws rounded to bf16, generated in chunks; returns uint16 bits."""
     n = int(np.prod(shape))
-    out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, _CHUNK):
-        e = min(n, s + _CHUNK)
-        out[s:e] = f32_to_bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
-    return out.reshape(shape)
+    return _chunked(rng, n, np.uint16, lambda g, c: f32_to_bf16_bits(
+        g.standard_normal(c, dtype=np.float32))).reshape(shape)
 
 
 @dataclasses.dataclass
@@ -181,12 +204,8 @@ def _fill_pool(rng, num_blocks, used_ids, Hkv, BS, D):
     k = np.full((num_blocks, Hkv, BS, D), NAN_BITS, dtype=np.uint16)
     v = np.full((num_blocks, Hkv, BS, D), NAN_BITS, dtype=np.uint16)
     used_ids = np.sort(np.asarray(used_ids))
-    # Generate block by block in chunks so temporaries stay bounded.
-    per = max(1, _CHUNK // (Hkv * BS * D))
-    for s in range(0, len(used_ids), per):
-        ids = used_ids[s:s + per]
-        k[ids] = normal_bf16(rng, (len(ids), Hkv, BS, D))
-        v[ids] = normal_bf16(rng, (len(ids), Hkv, BS, D))
+    k[used_ids] = normal_bf16(rng, (len(used_ids), Hkv, BS, D))
+    v[used_ids] = normal_bf16(rng, (len(used_ids), Hkv, BS, D))
     return k, v
 
 
@@ -262,14 +281,14 @@ def random_e4m3_codes(rng: np.random.Generator, shape, exp_lo=9, exp_hi=13) -> n
     """Random E4M3 bit patterns: uniform sign bit, exponent field uniform in
     [exp_lo, exp_hi], uniform 3-bit mantissa (no NaN code for exp_hi <= 14)."""
     n = int(np.prod(shape))
-    out = np.empty(n, dtype=np.uint8)
-    for s in range(0, n, _CHUNK):
-        e = min(n, s + _CHUNK)
-        sign = rng.integers(0, 2, e - s, dtype=np.uint8)
-        ex = rng.integers(exp_lo, exp_hi + 1, e - s, dtype=np.uint8)
-        man = rng.integers(0, 8, e - s, dtype=np.uint8)
-        out[s:e] = (sign << np.uint8(7)) | (ex << np.uint8(3)) | man
-    return out.reshape(shape)
+
+    def fill(g, c):
+        sign = g.integers(0, 2, c, dtype=np.uint8)
+        ex = g.integers(exp_lo, exp_hi + 1, c, dtype=np.uint8)
+        man = g.integers(0, 8, c, dtype=np.uint8)
+        return (sign << np.uint8(7)) | (ex << np.uint8(3)) | man
+
+    return _chunked(rng, n, np.uint8, fill).reshape(shape)
 
 
 def fp8_variant(w: Workload, seed: int = 0, scale_lo=1.0 / 96, scale_hi=1.0 / 48) -> Workload:
