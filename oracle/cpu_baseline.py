@@ -7,12 +7,15 @@ BLAS thread count can be pinned before NumPy loads:
     OPENBLAS_NUM_THREADS=1 OMP_NUM_THREADS=1 python -m oracle.cpu_baseline decode_8b 10
 
 prints one JSON object: KV bytes read by the oracle (unique pages of the
-sequences it processed), seconds, GB/s and the sample description.  A name
-ending in ``_fp8`` times the FP8-page oracle on that workload's FP8 variant
-(variant seed 0).  The
-workload's new tokens are scattered into the caches before timing; the timed
-work is the oracle's paged attention over whole sequences, in batch order,
-repeated over the batch until ``seconds`` have elapsed.
+sequences it processed), seconds, GB/s, the worker count and the sample
+description.  A name ending in ``_fp8`` times the FP8-page oracle on that
+workload's FP8 variant (variant seed 0).  The workload's new tokens are
+scattered into the caches before timing; the timed work is the oracle's paged
+attention over whole sequences.  It runs on every host core this process may
+use (one worker process per core, each with single-threaded BLAS): worker i
+takes sequences i, i + P, i + 2P, ... of the batch, wrapping, until ``seconds``
+have elapsed.  The workers are forked from this process, which never touches
+a GPU.
 """
 from __future__ import annotations
 
@@ -73,28 +76,77 @@ def run_seqs(w, k, v, seqs):
 
 
 def time_passes(w, k, v, seconds: float):
-    """Oracle passes over the batch, one sequence at a time, until ``seconds`` elapsed."""
+    """Oracle passes over the batch on one core, one sequence at a time, until ``seconds``
+    elapsed."""
+    return _worker_passes(w, k, v, seconds, 0, 1)
+
+
+def _worker_passes(w, k, v, seconds, first, stride):
     done = []
     t0 = time.perf_counter()
-    b = 0
+    b = first % w.num_seqs
     while not done or time.perf_counter() - t0 < seconds:
         run_seqs(w, k, v, [b])
         done.append(b)
-        b = (b + 1) % w.num_seqs
+        b = (b + stride) % w.num_seqs
     dt = time.perf_counter() - t0
     nbytes = sum(seq_bytes(w, [x]) for x in done)
     return {"bytes": nbytes, "seconds": dt, "gbps": nbytes / dt / 1e9, "seqs": len(done),
             "seq_steps_per_s": len(done) / dt}
 
 
+_STATE = {}
+
+
+def _pool_task(args):
+    first, stride, seconds = args
+    w, k, v = _STATE["wkv"]
+    return _worker_passes(w, k, v, seconds, first, stride)
+
+
+def _pool_seqs(seqs):
+    w, k, v = _STATE["wkv"]
+    return run_seqs(w, k, v, seqs)
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def make_pool(w, k, v, workers: int):
+    """A pool of ``workers`` processes forked from this (GPU-free) process, sharing the
+    prepared workload."""
+    import multiprocessing as mp
+    _STATE["wkv"] = (w, k, v)
+    return mp.get_context("fork").Pool(workers)
+
+
+def time_passes_parallel(w, k, v, seconds: float, workers: int):
+    """``workers`` processes run oracle passes for ``seconds`` each; GB/s over the slowest
+    worker's time."""
+    t0 = time.perf_counter()
+    with make_pool(w, k, v, workers) as pool:
+        parts = pool.map(_pool_task, [(i, workers, seconds) for i in range(workers)])
+    wall = time.perf_counter() - t0
+    nbytes = sum(p["bytes"] for p in parts)
+    nseq = sum(p["seqs"] for p in parts)
+    # Each worker stops after its own `seconds`; the slowest sets the wall time.
+    slowest = max(p["seconds"] for p in parts)
+    return {"bytes": nbytes, "seconds": slowest, "wall_seconds": wall,
+            "gbps": nbytes / slowest / 1e9, "seqs": nseq, "seq_steps_per_s": nseq / slowest}
+
+
 def main(argv):
     name = argv[1] if len(argv) > 1 else "decode_8b"
     seconds = float(argv[2]) if len(argv) > 2 else 10.0
+    workers = int(argv[3]) if len(argv) > 3 else host_cores()
     w, k, v = prepare(name)
-    r = time_passes(w, k, v, seconds)
-    r.update({"workload": name, "cores": threads_used(),
-              "sample": f"{r['seqs']} whole sequences of the {name} batch (batch order, "
-                        f"wrapping), fp64 paged attention; reshape_and_cache untimed"})
+    r = time_passes_parallel(w, k, v, seconds, workers)
+    r.update({"workload": name, "cores": workers,
+              "sample": f"{r['seqs']} whole sequences of the {name} batch, fp64 paged "
+                        f"attention on {workers} worker processes (one per host core, "
+                        f"single-threaded BLAS; worker i takes sequences i, i+{workers}, ..., "
+                        f"wrapping) for {seconds:g} s; reshape_and_cache untimed"})
     print(json.dumps(r))
 
 

@@ -265,31 +265,3 @@ def test_shared_prefix_read_once(psize):
     assert_close(out, ref, what=f"fp8 shared prefix ps{psize}")
     plain = d.attend(partition_size=psize)
     assert_close(out, plain.float().cpu().double().numpy(), what="fp8 shared vs plain")
-
-
-def sample_seqs(w, n=6, seed=0):
-    L = w.context_lens
-    pick = {int(np.argmin(L)), int(np.argmax(L))}
-    rng = np.random.default_rng(seed)
-    while len(pick) < min(n, w.num_seqs):
-        pick.add(int(rng.integers(w.num_seqs)))
-    return sorted(pick)
-
-
-@pytest.mark.parametrize("name", ["decode_8b", "decode_70b", "spec_verify"])
-def test_full_size_sampled(name):
-    """Full-size FP8 workloads in the benchmark's launch configuration (fused append,
-    default partitions); sampled rows vs the oracle."""
-    w = fp8(name, size="full")
-    d = Dev8(w)
-    out = d.attend_append()
-    torch.cuda.synchronize()
-    assert bool(torch.isfinite(out.float()).all())
-    seqs = sample_seqs(w)
-    k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
-                               w.k_scale, w.v_scale, 16)
-    ref = F.paged_attention(w.q, k, v, w.k_scale, w.v_scale, w.block_tables, w.context_lens,
-                            w.scale, w.num_kv_heads, 16, seqs=seqs)
-    assert_close(out, ref, seqs=seqs, what=f"{name} fp8 full")
-    s = w.slot_mapping
-    np.testing.assert_array_equal(codes(d.k)[s // 16, :, s % 16, :], k[s // 16, :, s % 16, :])

@@ -291,47 +291,6 @@ def test_wait_timeout_self_test():
     assert_close(d.attend(), ref, what="after timeout")
 
 
-# ----------------------------------------------------------------------------- full sizes
-
-def sample_seqs(w, n=6, seed=0):
-    L = w.context_lens
-    pick = {int(np.argmin(L)), int(np.argmax(L))}
-    rng = np.random.default_rng(seed)
-    while len(pick) < min(n, w.num_seqs):
-        pick.add(int(rng.integers(w.num_seqs)))
-    return sorted(pick)
-
-
-@pytest.mark.parametrize("name", ["tiny", "decode_8b", "decode_70b", "spec_verify",
-                                  "shared_prefix"])
-def test_full_size_sampled(name):
-    """Full-size workload in the benchmark's launch configuration; sampled rows vs the oracle.
-
-    The benchmark runs the fused append call for the per-sequence workloads and
-    reshape_and_cache + the shared-prefix call for the shared-prefix workload."""
-    w = W.FULL[name]()
-    d = Dev(w)
-    if w.seq_group is None:
-        out = d.attend_append()
-    else:
-        d.reshape()
-        out = d.attend()
-    torch.cuda.synchronize()
-    assert bool(torch.isfinite(out.float()).all())
-    seqs = sample_seqs(w, n=4 if name == "shared_prefix" else 6)
-    k = w.k_cache.copy()
-    v = w.v_cache.copy()
-    s = w.slot_mapping
-    k[s // 16, :, s % 16, :] = w.new_key
-    v[s // 16, :, s % 16, :] = w.new_value
-    ref = O.paged_attention(w.q, k, v, w.block_tables, w.context_lens, w.scale,
-                            w.num_kv_heads, 16, seqs=seqs)
-    assert_close(out, ref, seqs=seqs, what=f"{name} full")
-    # reshape_and_cache: every written slot holds its token, bit for bit
-    kb = bits(d.k)
-    np.testing.assert_array_equal(kb[s // 16, :, s % 16, :], w.new_key)
-
-
 # ----------------------------------------------------------------------------- softmax range
 
 def _f32(bits_u16):

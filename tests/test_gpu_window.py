@@ -8,6 +8,7 @@ import torch
 
 import workloads as W
 from oracle import window as WIN
+from oracle_threads import all_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -116,17 +117,16 @@ def test_negative_window_rejected():
 
 
 @pytest.mark.parametrize("name,window", [("spec_verify", 4096), ("decode_70b", 1024)])
-def test_full_size_sampled(name, window):
+def test_full_size_every_sequence(name, window):
     w = W.FULL[name]()
     d = Dev(w)
     out = attend(d, window, 0, True)
     torch.cuda.synchronize()
-    seqs = sorted({int(np.argmin(w.context_lens)), int(np.argmax(w.context_lens)), 3, 7})
     k = w.k_cache.copy()
     v = w.v_cache.copy()
     s = w.slot_mapping
     k[s // 16, :, s % 16, :] = w.new_key
     v[s // 16, :, s % 16, :] = w.new_value
-    ref = WIN.paged_attention(w.q, k, v, w.block_tables, w.context_lens, w.scale,
-                              w.num_kv_heads, 16, window, seqs=seqs)
-    assert_close(out, ref, seqs=seqs, what=f"{name} window {window} full")
+    ref = all_rows(WIN.paged_attention, w.num_seqs, w.q, k, v, w.block_tables, w.context_lens,
+                   w.scale, w.num_kv_heads, 16, window)
+    assert_close(out, ref, what=f"{name} window {window} full")
