@@ -1,7 +1,8 @@
 """Parity of the FP8 (E4M3) page path (through the C ABI) with the fp64 FP8 oracle.
 
 reshape_and_cache_fp8 is compared code for code over the whole pool.  Attention
-outputs (bf16) must be within max abs error 1e-2 and relative L2 error 2e-3 of
+outputs (bf16) must be within max abs error 1e-2 (or one bf16 ulp of the oracle
+value, where that is larger) and relative L2 error 2e-3 of
 attention over the dequantised pages in fp64.
 """
 import numpy as np
