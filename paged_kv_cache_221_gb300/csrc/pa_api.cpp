@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "paged_attn.h"
@@ -71,6 +72,17 @@ bool encode_fp8_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_base, const
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Multi-query tiles of 17-32 query rows per kv head (speculative verify) run on
+// the tcgen05 kernel unless PA_ATTN_MMA_SYNC=1 is set in the environment (read
+// once), which selects the mma.sync kernel for every tile, for comparison.
+bool tensor_core_kernel_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("PA_ATTN_MMA_SYNC");
+    return !(v != nullptr && v[0] == '1');
+  }();
+  return on;
+}
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
@@ -280,6 +292,8 @@ pa_status run_attention(const AttnArgs& a) {
     if (a.kv8)
       e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                            : launch_attn8_d128(tk, tv, p, rows, grid, a.stream, group_launch);
+    else if (a.head_dim == 128 && rows > 16 && rows <= 32 && tensor_core_kernel_enabled())
+      e = launch_attn_tc_d128(tk, tv, p, grid, a.stream, group_launch);
     else
       e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                            : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);
@@ -580,7 +594,7 @@ pa_status pa_get_device_error(pa_stream_t stream) {
       take_error_group_d128(&bits) != cudaSuccess || take_error_attn8_d64(&bits) != cudaSuccess ||
       take_error_attn8_d128(&bits) != cudaSuccess || take_error_group8_d64(&bits) != cudaSuccess ||
       take_error_group8_d128(&bits) != cudaSuccess || take_error_spec(&bits) != cudaSuccess ||
-      take_error_misc(&bits) != cudaSuccess)
+      take_error_attn_tc_d128(&bits) != cudaSuccess || take_error_misc(&bits) != cudaSuccess)
     return PA_ERR_CUDA;
   if (bits & kErrTimeout) return PA_ERR_TIMEOUT;
   if (bits & kErrBounds) return PA_ERR_BOUNDS;
