@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "paged_attn.h"
@@ -73,15 +74,13 @@ bool encode_fp8_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_base, const
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Multi-query tiles of 17-32 query rows per kv head (speculative verify) run on
-// the tcgen05 kernel unless PA_ATTN_MMA_SYNC=1 is set in the environment (read
-// once), which selects the mma.sync kernel for every tile, for comparison.
+// Kernel for multi-query tiles of 17-32 query rows per kv head (speculative
+// verify) at head_dim 128 with bf16 pages: the mma.sync kernel, or the tcgen05
+// kernel when the environment variable PA_VERIFY_KERNEL is "tcgen05" (read on
+// every call, so that a process can compare the two).
 bool tensor_core_kernel_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("PA_ATTN_MMA_SYNC");
-    return !(v != nullptr && v[0] == '1');
-  }();
-  return on;
+  const char* v = std::getenv("PA_VERIFY_KERNEL");
+  return v != nullptr && std::strcmp(v, "tcgen05") == 0;
 }
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }

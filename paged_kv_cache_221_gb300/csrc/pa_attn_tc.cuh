@@ -7,20 +7,29 @@
 // TMA.  Eight 16-token pages form one group of 128 tokens, the M dimension of
 // the score MMA:
 //
-//   S^T[128 tokens x 32 rows] = K[128 tokens x D] . Q^T[D x 32 rows]     (TMEM)
-//   O^T[D x 32 rows]         += V^T[D x 16 tokens] . P^T[16 tokens x 32 rows]
-//                               per page, P as a bf16 high part and a bf16
-//                               residual (two MMAs), so P keeps ~16 bits
+//   S^T[128 tokens x 32 row slots] = K[128 tokens x D] . Q^T[D x 32]      (TMEM)
+//   O^T[D x 64] += V^T[D x 16 tokens] . [P_hi^T | P_lo^T][16 tokens x 64] per page
 //
-// Both accumulators live in tensor memory.  Roles (192 threads):
-//   warps 0-3  softmax: thread i owns TMEM lane i, i.e. token i of the group
-//              (scores) and head dim i (output).  Per group: load the scores,
-//              mask, keep a per-row reference max that only moves when a score
-//              exceeds it by 8 (log2 units; then O is rescaled in TMEM), write
-//              P^T to shared memory, accumulate per-thread row sums.
-//   warp 4     producer: block-table lookup and TMA loads of K and V pages
-//              into a ring of kGroups groups (128-byte swizzle).
-//   warp 5     TMEM allocation; lane 0 issues every MMA and commits them to
+// P is split into a bf16 high part and a bf16 residual (so it keeps ~16 bits)
+// that sit side by side in one B operand: one MMA per page accumulates both
+// halves of O^T, which are added at the end.  Both accumulators live in tensor
+// memory.  Query rows are placed in two halves of 16 row slots (rows
+// 0 .. h-1 in slots 0 .. h-1, rows h .. n-1 in slots 16 .. 16+n-h-1, h = ceil(n/2)),
+// so that each half of the softmax warps carries an equal share.
+//
+// Roles (320 threads):
+//   warps 0-7  softmax: warp w reads TMEM lanes 32 (w % 4) .. +31 (tokens of a
+//              group for S, head dims for O) and the 16 row slots of half w / 4.
+//              Per group: load the scores, mask (pages wholly visible to every
+//              row skip it), keep a per-row reference max that moves only when
+//              a score exceeds it by 8 (log2 units; O is then rescaled in TMEM),
+//              write P^T (MN-major, 16-byte stores), accumulate row sums.
+//   warp 8     producer: block-table ids read ahead, TMA loads of K pages into
+//              a ring of kKGroups groups and of V pages into a ring of kVGroups
+//              groups (128-byte swizzle).  A group's K is free again once its
+//              scores are computed, its V once its P.V is, so K runs ahead.
+//   warp 9     TMEM allocation; lane 0 issues every MMA, whichever of the next
+//              score MMA and the next P.V is ready first, and commits them to
 //              mbarriers.
 // The K ring is laid out [head-dim half][ring page][16 tokens][128 B] so that
 // the 128 tokens of a group are one K-major operand with a uniform stride; V
@@ -40,35 +49,47 @@ namespace pa {
 struct TcGeo {
   static constexpr int D = 128;
   static constexpr int kGroupPages = 8;                  // pages per score MMA (M = 128)
-  static constexpr int kGroups = 2;                      // ring groups
-  static constexpr int kSlots = kGroups * kGroupPages;   // ring pages
-  static constexpr int kRows = 32;                       // N of both MMAs
+  static constexpr int kKGroups = 3;                     // K ring groups
+  static constexpr int kVGroups = 2;                     // V ring groups
+  static constexpr int kKSlots = kKGroups * kGroupPages; // K ring pages
+  static constexpr int kVSlots = kVGroups * kGroupPages; // V ring pages
+  static constexpr int kRows = 32;                       // N of the score MMA (row slots)
+  static constexpr int kHalfRows = 16;                   // row slots per softmax half
+  static constexpr int kSoftmaxWarps = 8;
+  static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
   static constexpr int kHalfBytes = kBlockSize * 128;    // 16 tokens x 64 dims bf16
+  // P^T operand, MN-major without swizzle: core matrices of 8 tokens x 8 row
+  // slots (8 rows of 16 bytes, one per token); token blocks kPKStride apart,
+  // row-slot blocks (hi slots 0-31, then lo slots 0-31) kPNStride apart
+  static constexpr int kPKStride = 128;
+  static constexpr int kPNStride = (kGroupPages * kBlockSize / 8) * kPKStride;   // 2048
+  static constexpr int kPBytes = 2 * kRows / 8 * kPNStride;                     // 16 KB
   // shared memory (offsets from a 1024-byte aligned base)
-  static constexpr int kKOff = 0;                                        // [2][kSlots][2048]
-  static constexpr int kVOff = kKOff + 2 * kSlots * kHalfBytes;          // [kSlots][2][2048]
-  static constexpr int kQOff = kVOff + 2 * kSlots * kHalfBytes;          // [2][32][128]
-  static constexpr int kPOff = kQOff + 2 * kRows * 128;                  // [2 buf][2 hi/lo][2][32][128]
-  static constexpr int kPBytes = 2 * kRows * 128;                        // one (buf, hi/lo) operand
-  static constexpr int kMiscOff = kPOff + 4 * kPBytes;
+  static constexpr int kKOff = 0;                                        // [2][kKSlots][2048]
+  static constexpr int kVOff = kKOff + 2 * kKSlots * kHalfBytes;         // [kVSlots][2][2048]
+  static constexpr int kQOff = kVOff + 2 * kVSlots * kHalfBytes;         // [2][32][128]
+  static constexpr int kPOff = kQOff + 2 * kRows * 128;                  // [2 buffers][16 KB]
+  static constexpr int kMiscOff = kPOff + 2 * kPBytes;
   static constexpr int kAlloc = kMiscOff + 2048 + 1024;
-  static constexpr uint32_t kTmemCols = 128;   // S buffers at 0 and 32, O at 64
+  static constexpr uint32_t kTmemCols = 128;   // S buffers at columns 0 and 32, O at 64
 };
 
 // Small shared state (barriers, flags, reduction buffers).
 struct TcMisc {
-  uint64_t kv_full[TcGeo::kGroups];
-  uint64_t kv_empty[TcGeo::kGroups];
+  uint64_t k_full[TcGeo::kKGroups];
+  uint64_t k_empty[TcGeo::kKGroups];         // completes after the score MMA of the group
+  uint64_t v_full[TcGeo::kVGroups];
+  uint64_t v_empty[TcGeo::kVGroups];         // completes after the P.V of the group
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t p_empty[2];                       // completes after the P.V of group h (buffer h & 1)
   uint64_t fin;
   uint32_t tmem_base;
-  int stage_ok[TcGeo::kSlots];
-  int lim[TcGeo::kRows];
-  int flag[2][4];
-  float red[4][TcGeo::kRows];
+  int stage_ok[4][TcGeo::kGroupPages];       // [group % 4][page]: loaded (for the P.V)
+  int lim[TcGeo::kRows];                     // per row slot: last visible position, -1 unused
+  int flag[2][2][4];                         // [S buffer][half][warp of the half]
+  float red[2][4][TcGeo::kHalfRows];
 };
 static_assert(sizeof(TcMisc) <= 2048, "misc area");
 
@@ -78,12 +99,20 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int byte_in_row) {
                                             (byte_in_row & 15)));
 }
 
-__global__ void __launch_bounds__(192, 1)
+// Two floats as a bf16x2 word, rounded to nearest even (`lo` in bits 0-15).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __launch_bounds__(TcGeo::kThreads, 1)
     paged_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
   using Gm = TcGeo;
   constexpr int D = Gm::D;
   constexpr int NR = Gm::kRows;
+  constexpr int NH = Gm::kHalfRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -116,6 +145,7 @@ __global__ void __launch_bounds__(192, 1)
   const int slot = npre + unit_p;
   const bool direct = (pre == 0 && nparts == 1);
   const int nrows = G * T;
+  const int hA = (nrows + 1) / 2;            // rows in the first half of the row slots
   const int npages = pg1 - pg0;
   const int ngroups = (npages + Gm::kGroupPages - 1) / Gm::kGroupPages;
   const int32_t* trow = p.block_tables + static_cast<size_t>(b) * p.mbs;
@@ -127,40 +157,46 @@ __global__ void __launch_bounds__(192, 1)
 
   // ------------------------------------------------------------------ setup
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Gm::kGroups; ++i) {
-      mbar_init(&ms.kv_full[i], 1);
-      mbar_init(&ms.kv_empty[i], 1);
+    for (int i = 0; i < Gm::kKGroups; ++i) {
+      mbar_init(&ms.k_full[i], 1);
+      mbar_init(&ms.k_empty[i], 1);
+    }
+    for (int i = 0; i < Gm::kVGroups; ++i) {
+      mbar_init(&ms.v_full[i], 1);
+      mbar_init(&ms.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms.s_full[i], 1);
-      mbar_init(&ms.s_free[i], 4);
-      mbar_init(&ms.p_full[i], 4);
+      mbar_init(&ms.s_free[i], Gm::kSoftmaxWarps);
+      mbar_init(&ms.p_full[i], Gm::kSoftmaxWarps);
       mbar_init(&ms.p_empty[i], 1);
     }
     mbar_init(&ms.fin, 1);
     fence_barrier_init();
   }
-  if (warp == 5) tc::tmem_alloc(&ms.tmem_base, Gm::kTmemCols);
-  if (warp < 4) {
-    // Q rows (zero rows pad to 32), K-major with the 128-byte swizzle:
-    // [dim half][row][128 B]
+  if (warp == Gm::kSoftmaxWarps + 1) tc::tmem_alloc(&ms.tmem_base, Gm::kTmemCols);
+  if (warp < Gm::kSoftmaxWarps) {
+    // Q rows in their row slots (unused slots zero), K-major with the 128-byte
+    // swizzle: [dim half][slot][128 B]
     constexpr int CH = D / 8;
-    for (int idx = threadIdx.x; idx < NR * CH; idx += 128) {
+    for (int idx = threadIdx.x; idx < NR * CH; idx += Gm::kSoftmaxWarps * 32) {
       const int n = idx / CH, ch = idx % CH;
+      const int r = n < NH ? n : hA + (n - NH);
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (n < nrows) {
-        const int t = n / G, hl = n % G;
+      if (n < NH ? n < hA : r < nrows) {
+        const int t = r / G, hl = r % G;
         const size_t row = (static_cast<size_t>(b) * T + t) * p.Hq + g * G + hl;
         v = reinterpret_cast<const uint4*>(p.q)[row * CH + ch];
       }
       *reinterpret_cast<uint4*>(smem + Gm::kQOff + (ch >> 3) * (NR * 128) +
                                 tc_sw128(n, (ch & 7) * 16)) = v;
     }
-    // P operands start at zero (rows >= nrows stay zero)
-    for (int idx = threadIdx.x; idx < 4 * Gm::kPBytes / 16; idx += 128)
-      reinterpret_cast<uint4*>(smem + Gm::kPOff)[idx] = make_uint4(0, 0, 0, 0);
-    if (threadIdx.x < NR)
-      ms.lim[threadIdx.x] = threadIdx.x < nrows ? L - T + static_cast<int>(threadIdx.x) / G : -1;
+    if (threadIdx.x < NR) {
+      const int n = threadIdx.x;
+      const int r = n < NH ? n : hA + (n - NH);
+      const bool used = n < NH ? n < hA : r < nrows;
+      ms.lim[n] = used ? L - T + r / G : -1;
+    }
     tc::fence_proxy_async_smem();
   }
   tc::fence_before_sync();
@@ -169,7 +205,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = ms.tmem_base;
   const uint32_t tmem_o = tmem + 64;
 
-  if (warp == 4) {
+  if (warp == Gm::kSoftmaxWarps) {
     // ---------------------------------------------------------------- producer
     // Query tokens' K/V that land in this unit's pages are stored first
     // (reshape_and_cache fused), then made visible to the TMA reads.
@@ -202,105 +238,144 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_map(&tmk);
       tma_prefetch_map(&tmv);
     }
+    // block ids of pages [32 i, 32 i + 32) in lane order, one batch read ahead
+    int ids_cur = lane < npages ? __ldg(trow + pg0 + lane) : 0;
+    int ids_nxt = 32 + lane < npages ? __ldg(trow + pg0 + 32 + lane) : 0;
     bool aborted = false;
     for (int grp = 0; grp < ngroups; ++grp) {
-      const int rb = grp % Gm::kGroups;
-      const uint32_t use = static_cast<uint32_t>(grp / Gm::kGroups);
-      if (!aborted && !mbar_wait(&ms.kv_empty[rb], (use & 1u) ^ 1u, p.timeout_ns)) aborted = true;
-      aborted = __any_sync(0xffffffffu, aborted);
-      const int pi = grp * Gm::kGroupPages + lane;
+      const int base = grp * Gm::kGroupPages;
+      if (grp > 0 && (base & 31) == 0) {
+        ids_cur = ids_nxt;
+        ids_nxt = base + 32 + lane < npages ? __ldg(trow + pg0 + base + 32 + lane) : 0;
+      }
+      const int phys = __shfl_sync(0xffffffffu, ids_cur, (base & 31) + (lane & 7));
+      const int pi = base + lane;
       const bool in = lane < Gm::kGroupPages && pi < npages;
-      const int phys = in ? __ldg(trow + pg0 + pi) : 0;
-      const bool ok = in && !aborted &&
-                      static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
-      if (in && static_cast<unsigned>(phys) >= static_cast<unsigned>(p.num_blocks))
-        atomicOr(&g_pa_err, kErrBounds);
-      const int sl = rb * Gm::kGroupPages + lane;
-      if (lane < Gm::kGroupPages) ms.stage_ok[sl] = ok ? 1 : 0;
+      const bool inpool = static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
+      if (in && !inpool) atomicOr(&g_pa_err, kErrBounds);
+      const int row = (phys * p.Hkv + g) * kBlockSize;
+      // K: free once the score MMA of group grp - kKGroups has completed
+      const int kb = grp % Gm::kKGroups;
+      const uint32_t ku = static_cast<uint32_t>(grp / Gm::kKGroups);
+      if (!aborted && !mbar_wait(&ms.k_empty[kb], (ku & 1u) ^ 1u, p.timeout_ns)) aborted = true;
+      aborted = __any_sync(0xffffffffu, aborted);
+      const bool ok = in && inpool && !aborted;
       const unsigned okm = __ballot_sync(0xffffffffu, ok);
-      __syncwarp();
       if (lane == 0)
-        mbar_arrive_expect_tx(&ms.kv_full[rb],
-                              static_cast<uint32_t>(__popc(okm)) * 4u * Gm::kHalfBytes);
+        mbar_arrive_expect_tx(&ms.k_full[kb],
+                              static_cast<uint32_t>(__popc(okm)) * 2u * Gm::kHalfBytes);
       __syncwarp();
       if (ok) {
-        const int row = (phys * p.Hkv + g) * kBlockSize;
-        uint8_t* kd = smem + Gm::kKOff + sl * Gm::kHalfBytes;
-        uint8_t* vd = smem + Gm::kVOff + sl * 2 * Gm::kHalfBytes;
-        tma_load_2d(kd, &tmk, &ms.kv_full[rb], 0, row);
-        tma_load_2d(kd + Gm::kSlots * Gm::kHalfBytes, &tmk, &ms.kv_full[rb], 64, row);
-        tma_load_2d(vd, &tmv, &ms.kv_full[rb], 0, row);
-        tma_load_2d(vd + Gm::kHalfBytes, &tmv, &ms.kv_full[rb], 64, row);
+        uint8_t* kd = smem + Gm::kKOff + (kb * Gm::kGroupPages + lane) * Gm::kHalfBytes;
+        tma_load_2d(kd, &tmk, &ms.k_full[kb], 0, row);
+        tma_load_2d(kd + Gm::kKSlots * Gm::kHalfBytes, &tmk, &ms.k_full[kb], 64, row);
+      }
+      // V: free once the P.V of group grp - kVGroups has completed
+      const int vb = grp % Gm::kVGroups;
+      const uint32_t vu = static_cast<uint32_t>(grp / Gm::kVGroups);
+      if (!aborted && !mbar_wait(&ms.v_empty[vb], (vu & 1u) ^ 1u, p.timeout_ns)) aborted = true;
+      aborted = __any_sync(0xffffffffu, aborted);
+      const bool okv = ok && !aborted;
+      const unsigned okvm = __ballot_sync(0xffffffffu, okv);
+      // which pages the P.V may use (read by the MMA thread after v_full; the P.V
+      // of group grp - 4, the previous reader of this entry, has completed)
+      if (lane < Gm::kGroupPages) ms.stage_ok[grp & 3][lane] = okv ? 1 : 0;
+      __syncwarp();
+      if (lane == 0)
+        mbar_arrive_expect_tx(&ms.v_full[vb],
+                              static_cast<uint32_t>(__popc(okvm)) * 2u * Gm::kHalfBytes);
+      __syncwarp();
+      if (okv) {
+        uint8_t* vd = smem + Gm::kVOff + (vb * Gm::kGroupPages + lane) * 2 * Gm::kHalfBytes;
+        tma_load_2d(vd, &tmv, &ms.v_full[vb], 0, row);
+        tma_load_2d(vd + Gm::kHalfBytes, &tmv, &ms.v_full[vb], 64, row);
       }
     }
     // Do not leave while copies issued by this warp may still be landing.
     if (lane == 0) {
-      for (int grp = max(0, ngroups - Gm::kGroups); grp < ngroups; ++grp)
-        mbar_wait(&ms.kv_full[grp % Gm::kGroups],
-                  static_cast<uint32_t>(grp / Gm::kGroups) & 1u, p.timeout_ns);
+      for (int grp = max(0, ngroups - Gm::kKGroups); grp < ngroups; ++grp)
+        mbar_wait(&ms.k_full[grp % Gm::kKGroups],
+                  static_cast<uint32_t>(grp / Gm::kKGroups) & 1u, p.timeout_ns);
+      for (int grp = max(0, ngroups - Gm::kVGroups); grp < ngroups; ++grp)
+        mbar_wait(&ms.v_full[grp % Gm::kVGroups],
+                  static_cast<uint32_t>(grp / Gm::kVGroups) & 1u, p.timeout_ns);
     }
-  } else if (warp == 5) {
+  } else if (warp == Gm::kSoftmaxWarps + 1) {
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t kIdQK = tc::idesc_f16<128, NR, false, false, true>();
-      constexpr uint32_t kIdPV = tc::idesc_f16<128, NR, true, false, true>();
+      constexpr uint32_t kIdPV = tc::idesc_f16<128, 2 * NR, true, true, true>();
       bool aborted = false;
       uint32_t any_pv = 0;
-      auto issue_pv = [&](int h) {
-        const int pb = h & 1;
-        const int rb = h % Gm::kGroups;
-        if (!aborted && !mbar_wait(&ms.p_full[pb], static_cast<uint32_t>(h >> 1) & 1u,
-                                   p.timeout_ns))
-          aborted = true;
-        tc::fence_after_sync();
-        if (!aborted) {
-          for (int j = 0; j < Gm::kGroupPages; ++j) {
-            const int sl = rb * Gm::kGroupPages + j;
-            if (h * Gm::kGroupPages + j >= npages || !ms.stage_ok[sl]) continue;
-            // A = V^T (MN-major): dims 64..127 one 2048-byte half further, tokens
-            // 8..15 one 1024-byte atom further
-            const uint64_t ad = tc::smem_desc(vring + sl * 2 * Gm::kHalfBytes, Gm::kHalfBytes,
-                                              1024);
-            // B = P^T stored as P[row][token] (K-major): this page's 16 tokens
-            const uint32_t pbase = psm + (pb * 2) * Gm::kPBytes + (j >> 2) * (NR * 128) +
-                                   (j & 3) * 32;
-            tc::mma_f16_ss(tmem_o, ad, tc::smem_desc(pbase, 16, 1024), kIdPV, any_pv);
-            tc::mma_f16_ss(tmem_o, ad, tc::smem_desc(pbase + Gm::kPBytes, 16, 1024), kIdPV, 1u);
-            any_pv = 1u;
-          }
-          tc::commit(&ms.kv_empty[rb]);
-          tc::commit(&ms.p_empty[pb]);
-        } else {
-          mbar_arrive(&ms.kv_empty[rb]);
-          mbar_arrive(&ms.p_empty[pb]);
-        }
-      };
-      for (int grp = 0; grp < ngroups; ++grp) {
-        const int rb = grp % Gm::kGroups;
-        const int sb = grp & 1;
-        if (!aborted && !mbar_wait(&ms.kv_full[rb], static_cast<uint32_t>(grp / Gm::kGroups) & 1u,
-                                   p.timeout_ns))
-          aborted = true;
-        if (!aborted && !mbar_wait(&ms.s_free[sb], (static_cast<uint32_t>(grp >> 1) & 1u) ^ 1u,
-                                   p.timeout_ns))
-          aborted = true;
-        tc::fence_after_sync();
-        if (!aborted) {
+      int qk = 0, pv = 0;                      // next score MMA, next P.V
+      unsigned long long t_prog = global_timer_ns();
+      while (pv < ngroups) {
+        bool prog = false;
+        // scores of group qk: K landed, its S buffer read out (group qk - 2), and
+        // at most one group ahead of the P.V (the S / P buffer pairs)
+        if (qk < ngroups && qk <= pv + 1 &&
+            tc::mbar_test(&ms.k_full[qk % Gm::kKGroups],
+                          static_cast<uint32_t>(qk / Gm::kKGroups) & 1u) &&
+            tc::mbar_test(&ms.s_free[qk & 1], (static_cast<uint32_t>(qk >> 1) & 1u) ^ 1u)) {
+          tc::fence_after_sync();
+          const int kb = qk % Gm::kKGroups;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = kring + (kk >> 2) * (Gm::kSlots * Gm::kHalfBytes) +
-                                rb * Gm::kGroupPages * Gm::kHalfBytes + (kk & 3) * 32;
+            const uint32_t ka = kring + (kk >> 2) * (Gm::kKSlots * Gm::kHalfBytes) +
+                                kb * Gm::kGroupPages * Gm::kHalfBytes + (kk & 3) * 32;
             const uint32_t qa = qsm + (kk >> 2) * (NR * 128) + (kk & 3) * 32;
-            tc::mma_f16_ss(tmem + sb * NR, tc::smem_desc(ka, 16, 1024),
+            tc::mma_f16_ss(tmem + (qk & 1) * NR, tc::smem_desc(ka, 16, 1024),
                            tc::smem_desc(qa, 16, 1024), kIdQK, kk > 0 ? 1u : 0u);
           }
-          tc::commit(&ms.s_full[sb]);
-        } else {
-          mbar_arrive(&ms.s_full[sb]);
+          tc::commit(&ms.k_empty[kb]);
+          tc::commit(&ms.s_full[qk & 1]);
+          ++qk;
+          prog = true;
         }
-        if (grp > 0) issue_pv(grp - 1);
+        // P.V of group pv: its P written and its V landed
+        if (pv < qk && tc::mbar_test(&ms.p_full[pv & 1], static_cast<uint32_t>(pv >> 1) & 1u) &&
+            tc::mbar_test(&ms.v_full[pv % Gm::kVGroups],
+                          static_cast<uint32_t>(pv / Gm::kVGroups) & 1u)) {
+          tc::fence_after_sync();
+          const int vb = pv % Gm::kVGroups;
+          const int pb = pv & 1;
+          for (int j = 0; j < Gm::kGroupPages; ++j) {
+            if (pv * Gm::kGroupPages + j >= npages || !ms.stage_ok[pv & 3][j]) continue;
+            const int sl = vb * Gm::kGroupPages + j;
+            // A = V^T (MN-major, 128-byte swizzle): dims 64..127 one 2048-byte half
+            // further (leading offset), tokens 8..15 one 1024-byte atom further
+            const uint64_t ad = tc::smem_desc(vring + sl * 2 * Gm::kHalfBytes, Gm::kHalfBytes,
+                                              1024);
+            // B = [P_hi^T | P_lo^T] (MN-major, no swizzle): this page's two token
+            // blocks (leading offset), row-slot blocks kPNStride apart (stride offset)
+            const uint64_t bd = tc::smem_desc(psm + pb * Gm::kPBytes + j * 2 * Gm::kPKStride,
+                                              Gm::kPKStride, Gm::kPNStride, tc::kSwizzleNone);
+            tc::mma_f16_ss(tmem_o, ad, bd, kIdPV, any_pv);
+            any_pv = 1u;
+          }
+          tc::commit(&ms.v_empty[vb]);
+          tc::commit(&ms.p_empty[pb]);
+          ++pv;
+          prog = true;
+        }
+        if (prog) {
+          t_prog = global_timer_ns();
+        } else if (global_timer_ns() - t_prog > p.timeout_ns) {
+          atomicOr(&g_pa_err, kErrTimeout);
+          aborted = true;
+        }
+        if (aborted) {
+          // release whoever waits on the rest (their own waits are bounded too)
+          for (; qk < ngroups; ++qk) {
+            mbar_arrive(&ms.k_empty[qk % Gm::kKGroups]);
+            mbar_arrive(&ms.s_full[qk & 1]);
+          }
+          for (; pv < ngroups; ++pv) {
+            mbar_arrive(&ms.v_empty[pv % Gm::kVGroups]);
+            mbar_arrive(&ms.p_empty[pv & 1]);
+          }
+        }
       }
-      if (ngroups > 0) issue_pv(ngroups - 1);
       // every MMA of this unit has completed before the CTA may release TMEM
       tc::commit(&ms.fin);
       mbar_wait(&ms.fin, 0, p.timeout_ns);
@@ -308,126 +383,158 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax
-    const int t = threadIdx.x;                 // TMEM lane: token of the group, head dim
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const int q = warp & 3;                    // TMEM lane quarter
+    const int hf = warp >> 2;                  // row-slot half
+    const int t = q * 32 + lane;               // token of the group; head dim for O
+    const int cnt = hf == 0 ? hA : nrows - hA; // rows of this half
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const float sl2 = p.scale_log2;
-    float m[NR], lp[NR];
+    const int bar = 1 + hf;                    // named barrier of this half's 4 warps
+    float m[NH], lp[NH], thr[NH];
+    int lim[NH];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      m[r] = -CUDART_INF_F;
-      lp[r] = 0.f;
+    for (int k = 0; k < NH; ++k) {
+      m[k] = -CUDART_INF_F;
+      thr[k] = -CUDART_INF_F;
+      lp[k] = 0.f;
+      lim[k] = ms.lim[hf * NH + k];
     }
-    int lim[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) lim[r] = ms.lim[r];
+    const int minlim = L - T;                  // every row sees positions <= L - T
+    const bool nowin = p.window <= 0;
     bool aborted = false;
-    bool pv_before = false;                    // a valid page was in an earlier group
+    bool pv_before = false;                    // O holds data of an earlier group
     const int tail_tok = L - (pg0 + npages - 1) * kBlockSize;   // valid tokens of the last page
+    // block id of this thread's page in the next group, read one group ahead
+    int id_next = t / 16 < npages ? __ldg(trow + pg0 + t / 16) : -1;
     for (int grp = 0; grp < ngroups; ++grp) {
-      const int rb = grp % Gm::kGroups;
       const int sb = grp & 1;
-      if (!aborted && !mbar_wait(&ms.kv_full[rb], static_cast<uint32_t>(grp / Gm::kGroups) & 1u,
-                                 p.timeout_ns))
-        aborted = true;
+      const int pidx = grp * Gm::kGroupPages + (t >> 4);
+      const int id = id_next;
+      id_next = pidx + Gm::kGroupPages < npages ? __ldg(trow + pg0 + pidx + Gm::kGroupPages) : -1;
       if (!aborted && !mbar_wait(&ms.s_full[sb], static_cast<uint32_t>(grp >> 1) & 1u,
                                  p.timeout_ns))
         aborted = true;
       aborted = __any_sync(0xffffffffu, aborted);
       tc::fence_after_sync();
-      uint32_t sr[32];
-      tc::tmem_ld32(tmem + lane_addr + sb * NR, sr);
+      uint32_t sr[NH];
+      tc::tmem_ld16(tmem + lane_addr + sb * NR + hf * NH, sr);
       tc::tmem_wait_ld();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms.s_free[sb]);
 
-      const int pidx = grp * Gm::kGroupPages + (t >> 4);
-      const int sl = rb * Gm::kGroupPages + (t >> 4);
-      const bool valid = !aborted && pidx < npages && ms.stage_ok[sl] != 0;
+      // a page outside the unit or naming a block outside the pool is not loaded:
+      // its scores are masked and the MMA thread skips its P.V
+      const bool valid = !aborted && pidx < npages &&
+                         static_cast<unsigned>(id) < static_cast<unsigned>(p.num_blocks);
       const int j = (pg0 + pidx) * kBlockSize + (t & 15);
-      float x[NR];
+      const bool interior = valid && nowin && j <= minlim;
+      float x[NH];
       bool exceed = false;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const bool vis = valid && r < nrows &&
-                         static_cast<unsigned>(lim[r] - j) < p.wcap;
-        x[r] = vis ? __uint_as_float(sr[r]) * sl2 : -CUDART_INF_F;
-        exceed |= x[r] > m[r] + 8.f;
+      for (int k = 0; k < NH; ++k) {
+        const bool vis = k < cnt && (interior || (valid &&
+                         static_cast<unsigned>(lim[k] - j) < p.wcap));
+        x[k] = vis ? __uint_as_float(sr[k]) * sl2 : -CUDART_INF_F;
+        exceed |= x[k] > thr[k];
       }
-      // group-wide decision on moving the reference maxima
+      // decision of this half on moving its rows' reference maxima
+      // (bit 0: some score of the warp exceeds its row's threshold; bit 1: the
+      // warp's two pages include a loaded one)
       const bool wexceed = __any_sync(0xffffffffu, exceed);
-      if (lane == 0) ms.flag[sb][warp] = wexceed ? 1 : 0;
-      named_bar_sync(1, 128);
-      const bool any = (ms.flag[sb][0] | ms.flag[sb][1] | ms.flag[sb][2] | ms.flag[sb][3]) != 0;
+      const bool wvalid = __any_sync(0xffffffffu, valid);
+      if (lane == 0) ms.flag[sb][hf][q] = (wexceed ? 1 : 0) | (wvalid ? 2 : 0);
+      named_bar_sync(bar, 128);
+      const int fl = ms.flag[sb][hf][0] | ms.flag[sb][hf][1] | ms.flag[sb][hf][2] |
+                     ms.flag[sb][hf][3];
+      const bool any = (fl & 1) != 0;
       if (any) {
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          float v = x[r];
+        for (int k = 0; k < NH; ++k) {
+          float v = x[k];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-          if (lane == 0) ms.red[warp][r] = v;
+          if (lane == 0) ms.red[hf][q][k] = v;
         }
-        named_bar_sync(1, 128);
-        float alpha[NR];
+        named_bar_sync(bar, 128);
+        float alpha[NH];
         bool need_o = false;
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          const float mx = fmaxf(fmaxf(ms.red[0][r], ms.red[1][r]),
-                                 fmaxf(ms.red[2][r], ms.red[3][r]));
-          alpha[r] = 1.f;
-          if (mx > m[r] + 8.f) {
-            if (m[r] != -CUDART_INF_F) {
-              alpha[r] = hw_exp2(m[r] - mx);
+        for (int k = 0; k < NH; ++k) {
+          const float mx = fmaxf(fmaxf(ms.red[hf][0][k], ms.red[hf][1][k]),
+                                 fmaxf(ms.red[hf][2][k], ms.red[hf][3][k]));
+          alpha[k] = 1.f;
+          if (mx > thr[k]) {
+            if (m[k] != -CUDART_INF_F) {
+              alpha[k] = hw_exp2(m[k] - mx);
               need_o = true;
             } else {
-              alpha[r] = 0.f;
+              alpha[k] = 0.f;
             }
-            m[r] = mx;
+            m[k] = mx;
+            thr[k] = mx + 8.f;
           }
-          lp[r] *= alpha[r];
+          lp[k] *= alpha[k];
         }
-        named_bar_sync(1, 128);                // red[] may be rewritten next group
+        named_bar_sync(bar, 128);              // red[] may be rewritten next group
         if (need_o && pv_before && !aborted) {
           // O holds the pages of earlier groups: wait for their P.V (group grp - 1,
           // whose buffer's previous P.V, of group grp - 3, this thread already
-          // waited for), then rescale in TMEM
+          // waited for), then rescale this half's columns in TMEM
           if (!mbar_wait(&ms.p_empty[(grp - 1) & 1], static_cast<uint32_t>((grp - 1) >> 1) & 1u,
                          p.timeout_ns))
             aborted = true;
           aborted = __any_sync(0xffffffffu, aborted);
           tc::fence_after_sync();
-          uint32_t orr[32];
-          tc::tmem_ld32(tmem_o + lane_addr, orr);
+          uint32_t oh[NH], ol[NH];
+          tc::tmem_ld16(tmem_o + lane_addr + hf * NH, oh);
+          tc::tmem_ld16(tmem_o + lane_addr + NR + hf * NH, ol);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int r = 0; r < NR; ++r) orr[r] = __float_as_uint(__uint_as_float(orr[r]) * alpha[r]);
-          tc::tmem_st32(tmem_o + lane_addr, orr);
+          for (int k = 0; k < NH; ++k) {
+            oh[k] = __float_as_uint(__uint_as_float(oh[k]) * alpha[k]);
+            ol[k] = __float_as_uint(__uint_as_float(ol[k]) * alpha[k]);
+          }
+          tc::tmem_st16(tmem_o + lane_addr + hf * NH, oh);
+          tc::tmem_st16(tmem_o + lane_addr + NR + hf * NH, ol);
           tc::tmem_wait_st();
         }
       }
-      // P^T for this group: bf16 high part and residual, [row][token] swizzled
+      // weights, row sums, and P^T as two bf16 parts (MN-major: one 16-byte row
+      // of 8 row slots per token and core matrix)
+      uint32_t hi[NH / 2], lo[NH / 2];
+#pragma unroll
+      for (int k = 0; k < NH; k += 2) {
+        const float m0 = m[k] == -CUDART_INF_F ? 0.f : m[k];
+        const float m1 = m[k + 1] == -CUDART_INF_F ? 0.f : m[k + 1];
+        const float p0 = hw_exp2(x[k] - m0), p1 = hw_exp2(x[k + 1] - m1);
+        lp[k] += p0;
+        lp[k + 1] += p1;
+        const uint32_t h2 = pack_bf16x2(p0, p1);
+        hi[k / 2] = h2;
+        lo[k / 2] = pack_bf16x2(p0 - __uint_as_float(h2 << 16),
+                                p1 - __uint_as_float(h2 & 0xFFFF0000u));
+      }
       const int pb = grp & 1;
       if (!aborted && !mbar_wait(&ms.p_empty[pb], (static_cast<uint32_t>(grp >> 1) & 1u) ^ 1u,
                                  p.timeout_ns))
         aborted = true;
-      uint8_t* ph = smem + Gm::kPOff + (pb * 2) * Gm::kPBytes + (t >> 6) * (NR * 128);
-      uint8_t* plo = ph + Gm::kPBytes;
-      const int tb = (t & 63) * 2;
+      uint8_t* pt = smem + Gm::kPOff + pb * Gm::kPBytes + (t >> 3) * Gm::kPKStride + (t & 7) * 16;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (r >= nrows) break;
-        const float mr = m[r] == -CUDART_INF_F ? 0.f : m[r];
-        const float pr = hw_exp2(x[r] - mr);
-        lp[r] += pr;
-        const __nv_bfloat16 h = __float2bfloat16_rn(pr);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(pr - __bfloat162float(h));
-        const uint32_t off = tc_sw128(r, tb);
-        *reinterpret_cast<__nv_bfloat16*>(ph + off) = h;
-        *reinterpret_cast<__nv_bfloat16*>(plo + off) = lo;
+      for (int c = 0; c < NH / 8; ++c) {
+        *reinterpret_cast<uint4*>(pt + (2 * hf + c) * Gm::kPNStride) =
+            make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+        *reinterpret_cast<uint4*>(pt + (NR / 8 + 2 * hf + c) * Gm::kPNStride) =
+            make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
       }
       // V rows past the context end in the last page may hold anything (even
-      // NaN); their weight is 0, but 0 * NaN is NaN: zero them before the P.V.
-      if (pidx == npages - 1 && (t & 15) >= tail_tok && ms.stage_ok[sl] != 0) {
+      // NaN); their weight is 0, but 0 * NaN is NaN: zero them once they have
+      // landed, before the P.V.  (The V buffer of this group is refilled only
+      // after this group's P.V, so its barrier phase cannot run ahead.)
+      if (hf == 0 && pidx == npages - 1 && (t & 15) >= tail_tok && valid &&
+          mbar_wait(&ms.v_full[grp % Gm::kVGroups],
+                    static_cast<uint32_t>(grp / Gm::kVGroups) & 1u, p.timeout_ns)) {
+        const int sl = (grp % Gm::kVGroups) * Gm::kGroupPages + (t >> 4);
         uint4* vrow = reinterpret_cast<uint4*>(smem + Gm::kVOff + sl * 2 * Gm::kHalfBytes +
                                                (t & 15) * 128);
 #pragma unroll
@@ -438,10 +545,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       // the MMA thread issues P.V for every page of the group that is in the unit
       // and was loaded: from the next group on, O holds data
-#pragma unroll
-      for (int jj = 0; jj < Gm::kGroupPages; ++jj)
-        pv_before |= grp * Gm::kGroupPages + jj < npages &&
-                     ms.stage_ok[rb * Gm::kGroupPages + jj] != 0;
+      pv_before |= (fl & 2) != 0;
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
@@ -456,31 +560,34 @@ __global__ void __launch_bounds__(192, 1)
       aborted = true;
     aborted = __any_sync(0xffffffffu, aborted);
     tc::fence_after_sync();
-    uint32_t orr[32];
-    tc::tmem_ld32(tmem_o + lane_addr, orr);
+    uint32_t oh[NH], ol[NH];
+    tc::tmem_ld16(tmem_o + lane_addr + hf * NH, oh);
+    tc::tmem_ld16(tmem_o + lane_addr + NR + hf * NH, ol);
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      float v = lp[r];
+    for (int k = 0; k < NH; ++k) {
+      float v = lp[k];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) ms.red[warp][r] = v;
+      if (lane == 0) ms.red[hf][q][k] = v;
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(bar, 128);
     const int d = t;                           // head dim of this thread's O^T lane
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      if (r >= nrows) break;
-      const float Ls = ms.red[0][r] + ms.red[1][r] + ms.red[2][r] + ms.red[3][r];
+    for (int k = 0; k < NH; ++k) {
+      if (k >= cnt) break;
+      const float Ls = ms.red[hf][0][k] + ms.red[hf][1][k] + ms.red[hf][2][k] + ms.red[hf][3][k];
+      const int r = hf == 0 ? k : hA + k;
       const int tq = r / G, hl = r % G;
       const size_t orow = (static_cast<size_t>(b) * T + tq) * p.Hq + g * G + hl;
-      const float o = Ls > 0.f ? __uint_as_float(orr[r]) / Ls : 0.f;
+      const float osum = __uint_as_float(oh[k]) + __uint_as_float(ol[k]);
+      const float o = Ls > 0.f ? osum / Ls : 0.f;
       if (direct) {
         reinterpret_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(o);
       } else {
         const size_t pidx2 = orow * p.max_parts + slot;
         p.part_o[pidx2 * D + d] = o;
-        if (d == 0) p.part_ml[pidx2] = make_float2(m[r], Ls);
+        if (d == 0) p.part_ml[pidx2] = make_float2(m[k], Ls);
       }
     }
   }
@@ -488,7 +595,7 @@ __global__ void __launch_bounds__(192, 1)
   // ------------------------------------------------------------------ teardown
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == Gm::kSoftmaxWarps + 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, Gm::kTmemCols);
     tc::tmem_relinquish();
@@ -511,7 +618,7 @@ inline cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(TcGeo::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -32,7 +32,9 @@ LENS = [17, 100, 127, 128, 129, 255, 256, 257, 1000, 1023, 1024, 1025, 2047, 204
 
 
 @pytest.fixture(autouse=True)
-def no_device_error():
+def tcgen05_kernel(monkeypatch):
+    """Route 17-32-row tiles to the tcgen05 kernel for every test of this file."""
+    monkeypatch.setenv("PA_VERIFY_KERNEL", "tcgen05")
     yield
     assert pa.get_device_error() == 0, "device error word was set"
 
