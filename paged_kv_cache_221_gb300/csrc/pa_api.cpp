@@ -292,7 +292,7 @@ pa_status run_attention(const AttnArgs& a) {
       e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                            : launch_attn8_d128(tk, tv, p, rows, grid, a.stream, group_launch);
     else if (a.head_dim == 128 && rows > 16 && rows <= 32 && tensor_core_kernel_enabled())
-      e = launch_attn_tc_d128(tk, tv, p, grid, a.stream, group_launch);
+      e = launch_attn_tc_d128(tk, tv, p, rows, grid, a.stream, group_launch);
     else
       e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                            : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);

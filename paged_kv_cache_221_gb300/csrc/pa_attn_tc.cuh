@@ -17,17 +17,18 @@
 // 0 .. h-1 in slots 0 .. h-1, rows h .. n-1 in slots 16 .. 16+n-h-1, h = ceil(n/2)),
 // so that each half of the softmax warps carries an equal share.
 //
-// Roles (320 threads):
+// Roles (352 threads):
 //   warps 0-7  softmax: warp w reads TMEM lanes 32 (w % 4) .. +31 (tokens of a
 //              group for S, head dims for O) and the 16 row slots of half w / 4.
 //              Per group: load the scores, mask (pages wholly visible to every
 //              row skip it), keep a per-row reference max that moves only when
 //              a score exceeds it by 8 (log2 units; O is then rescaled in TMEM),
 //              write P^T (MN-major, 16-byte stores), accumulate row sums.
-//   warp 8     producer: block-table ids read ahead, TMA loads of K pages into
-//              a ring of kKGroups groups and of V pages into a ring of kVGroups
-//              groups (128-byte swizzle).  A group's K is free again once its
-//              scores are computed, its V once its P.V is, so K runs ahead.
+//   warps 8,10 producers: block-table ids read ahead, TMA loads of K pages
+//              (warp 8) into a ring of kKGroups groups and of V pages (warp 10)
+//              into a ring of kVGroups groups (128-byte swizzle).  A group's K
+//              is free again once its scores are computed, its V once its P.V
+//              is, so K runs ahead.
 //   warp 9     TMEM allocation; lane 0 issues every MMA, whichever of the next
 //              score MMA and the next P.V is ready first, and commits them to
 //              mbarriers.
@@ -50,13 +51,13 @@ struct TcGeo {
   static constexpr int D = 128;
   static constexpr int kGroupPages = 8;                  // pages per score MMA (M = 128)
   static constexpr int kKGroups = 3;                     // K ring groups
-  static constexpr int kVGroups = 2;                     // V ring groups
+  static constexpr int kVGroups = 3;                     // V ring groups
   static constexpr int kKSlots = kKGroups * kGroupPages; // K ring pages
   static constexpr int kVSlots = kVGroups * kGroupPages; // V ring pages
   static constexpr int kRows = 32;                       // N of the score MMA (row slots)
   static constexpr int kHalfRows = 16;                   // row slots per softmax half
   static constexpr int kSoftmaxWarps = 8;
-  static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+  static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
   static constexpr int kHalfBytes = kBlockSize * 128;    // 16 tokens x 64 dims bf16
   // P^T operand, MN-major without swizzle: core matrices of 8 tokens x 8 row
   // slots (8 rows of 16 bytes, one per token); token blocks kPKStride apart,
@@ -68,8 +69,8 @@ struct TcGeo {
   static constexpr int kKOff = 0;                                        // [2][kKSlots][2048]
   static constexpr int kVOff = kKOff + 2 * kKSlots * kHalfBytes;         // [kVSlots][2][2048]
   static constexpr int kQOff = kVOff + 2 * kVSlots * kHalfBytes;         // [2][32][128]
-  static constexpr int kPOff = kQOff + 2 * kRows * 128;                  // [2 buffers][16 KB]
-  static constexpr int kMiscOff = kPOff + 2 * kPBytes;
+  static constexpr int kPOff = kQOff + 2 * kRows * 128;                  // [16 KB]
+  static constexpr int kMiscOff = kPOff + kPBytes;
   static constexpr int kAlloc = kMiscOff + 2048 + 1024;
   static constexpr uint32_t kTmemCols = 128;   // S buffers at columns 0 and 32, O at 64
 };
@@ -83,7 +84,7 @@ struct TcMisc {
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
-  uint64_t p_empty[2];                       // completes after the P.V of group h (buffer h & 1)
+  uint64_t p_empty;                          // completes after the P.V of each group, in order
   uint64_t fin;
   uint32_t tmem_base;
   int stage_ok[4][TcGeo::kGroupPages];       // [group % 4][page]: loaded (for the P.V)
@@ -106,6 +107,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// NA: row slots per half that can hold a row (even, <= 16): 10 covers up to
+// 20 query rows per kv head, 16 up to 32.
+template <int NA>
 __global__ void __launch_bounds__(TcGeo::kThreads, 1)
     paged_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -113,6 +117,7 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
   constexpr int D = Gm::D;
   constexpr int NR = Gm::kRows;
   constexpr int NH = Gm::kHalfRows;
+  static_assert(NA % 2 == 0 && NA <= NH, "active row slots");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -169,8 +174,8 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
       mbar_init(&ms.s_full[i], 1);
       mbar_init(&ms.s_free[i], Gm::kSoftmaxWarps);
       mbar_init(&ms.p_full[i], Gm::kSoftmaxWarps);
-      mbar_init(&ms.p_empty[i], 1);
     }
+    mbar_init(&ms.p_empty, 1);
     mbar_init(&ms.fin, 1);
     fence_barrier_init();
   }
@@ -205,10 +210,13 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
   const uint32_t tmem = ms.tmem_base;
   const uint32_t tmem_o = tmem + 64;
 
-  if (warp == Gm::kSoftmaxWarps) {
-    // ---------------------------------------------------------------- producer
-    // Query tokens' K/V that land in this unit's pages are stored first
-    // (reshape_and_cache fused), then made visible to the TMA reads.
+  if (warp == Gm::kSoftmaxWarps || warp == Gm::kSoftmaxWarps + 2) {
+    // ---------------------------------------------------------------- producers
+    // One warp streams the K pages, another the V pages, so that K (free again
+    // as soon as a group's scores are computed) runs up to kKGroups groups ahead.
+    const bool isv = warp == Gm::kSoftmaxWarps + 2;
+    // Query tokens' K (V) that land in this unit's pages are stored first
+    // (reshape_and_cache fused), then made visible to this warp's TMA reads.
     if (p.new_k != nullptr) {
       const int jlo = max(0, (L - T) / kBlockSize - pg0);
       const int jhi = min(npages - 1, (L - 1) / kBlockSize - pg0);
@@ -222,22 +230,20 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
           const size_t dst = (static_cast<size_t>(phys) * p.Hkv + g) * kBlockSize +
                              (pos & (kBlockSize - 1));
           constexpr int CH = D / 8;
-          for (int c = lane; c < 2 * CH; c += 32) {
-            const bool isv = c >= CH;
-            const int cc = isv ? c - CH : c;
-            const uint4 v =
-                reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + cc];
-            reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + cc] = v;
+          if (lane < CH) {
+            const uint4 v = reinterpret_cast<const uint4*>(isv ? p.new_v : p.new_k)[src * CH + lane];
+            reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst * CH + lane] = v;
           }
         }
       }
       fence_proxy_async_global();
       __syncwarp();
     }
-    if (lane == 0) {
-      tma_prefetch_map(&tmk);
-      tma_prefetch_map(&tmv);
-    }
+    if (lane == 0) tma_prefetch_map(isv ? &tmv : &tmk);
+    constexpr int NGK = Gm::kKGroups, NGV = Gm::kVGroups;
+    const int ngr = isv ? NGV : NGK;
+    uint64_t* fullb = isv ? ms.v_full : ms.k_full;
+    uint64_t* emptyb = isv ? ms.v_empty : ms.k_empty;
     // block ids of pages [32 i, 32 i + 32) in lane order, one batch read ahead
     int ids_cur = lane < npages ? __ldg(trow + pg0 + lane) : 0;
     int ids_nxt = 32 + lane < npages ? __ldg(trow + pg0 + 32 + lane) : 0;
@@ -252,53 +258,40 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
       const int pi = base + lane;
       const bool in = lane < Gm::kGroupPages && pi < npages;
       const bool inpool = static_cast<unsigned>(phys) < static_cast<unsigned>(p.num_blocks);
-      if (in && !inpool) atomicOr(&g_pa_err, kErrBounds);
-      const int row = (phys * p.Hkv + g) * kBlockSize;
-      // K: free once the score MMA of group grp - kKGroups has completed
-      const int kb = grp % Gm::kKGroups;
-      const uint32_t ku = static_cast<uint32_t>(grp / Gm::kKGroups);
-      if (!aborted && !mbar_wait(&ms.k_empty[kb], (ku & 1u) ^ 1u, p.timeout_ns)) aborted = true;
+      if (isv && in && !inpool) atomicOr(&g_pa_err, kErrBounds);
+      // the buffer is free once the score MMA (K) or the P.V (V) of group
+      // grp - ngr has completed
+      const int rb = grp % ngr;
+      const uint32_t use = static_cast<uint32_t>(grp / ngr);
+      if (!aborted && !mbar_wait(&emptyb[rb], (use & 1u) ^ 1u, p.timeout_ns)) aborted = true;
       aborted = __any_sync(0xffffffffu, aborted);
       const bool ok = in && inpool && !aborted;
       const unsigned okm = __ballot_sync(0xffffffffu, ok);
-      if (lane == 0)
-        mbar_arrive_expect_tx(&ms.k_full[kb],
-                              static_cast<uint32_t>(__popc(okm)) * 2u * Gm::kHalfBytes);
-      __syncwarp();
-      if (ok) {
-        uint8_t* kd = smem + Gm::kKOff + (kb * Gm::kGroupPages + lane) * Gm::kHalfBytes;
-        tma_load_2d(kd, &tmk, &ms.k_full[kb], 0, row);
-        tma_load_2d(kd + Gm::kKSlots * Gm::kHalfBytes, &tmk, &ms.k_full[kb], 64, row);
-      }
-      // V: free once the P.V of group grp - kVGroups has completed
-      const int vb = grp % Gm::kVGroups;
-      const uint32_t vu = static_cast<uint32_t>(grp / Gm::kVGroups);
-      if (!aborted && !mbar_wait(&ms.v_empty[vb], (vu & 1u) ^ 1u, p.timeout_ns)) aborted = true;
-      aborted = __any_sync(0xffffffffu, aborted);
-      const bool okv = ok && !aborted;
-      const unsigned okvm = __ballot_sync(0xffffffffu, okv);
       // which pages the P.V may use (read by the MMA thread after v_full; the P.V
       // of group grp - 4, the previous reader of this entry, has completed)
-      if (lane < Gm::kGroupPages) ms.stage_ok[grp & 3][lane] = okv ? 1 : 0;
+      if (isv && lane < Gm::kGroupPages) ms.stage_ok[grp & 3][lane] = ok ? 1 : 0;
       __syncwarp();
       if (lane == 0)
-        mbar_arrive_expect_tx(&ms.v_full[vb],
-                              static_cast<uint32_t>(__popc(okvm)) * 2u * Gm::kHalfBytes);
+        mbar_arrive_expect_tx(&fullb[rb], static_cast<uint32_t>(__popc(okm)) * 2u * Gm::kHalfBytes);
       __syncwarp();
-      if (okv) {
-        uint8_t* vd = smem + Gm::kVOff + (vb * Gm::kGroupPages + lane) * 2 * Gm::kHalfBytes;
-        tma_load_2d(vd, &tmv, &ms.v_full[vb], 0, row);
-        tma_load_2d(vd + Gm::kHalfBytes, &tmv, &ms.v_full[vb], 64, row);
+      if (ok) {
+        const int row = (phys * p.Hkv + g) * kBlockSize;
+        const int sl = rb * Gm::kGroupPages + lane;
+        if (isv) {
+          uint8_t* vd = smem + Gm::kVOff + sl * 2 * Gm::kHalfBytes;
+          tma_load_2d(vd, &tmv, &fullb[rb], 0, row);
+          tma_load_2d(vd + Gm::kHalfBytes, &tmv, &fullb[rb], 64, row);
+        } else {
+          uint8_t* kd = smem + Gm::kKOff + sl * Gm::kHalfBytes;
+          tma_load_2d(kd, &tmk, &fullb[rb], 0, row);
+          tma_load_2d(kd + Gm::kKSlots * Gm::kHalfBytes, &tmk, &fullb[rb], 64, row);
+        }
       }
     }
     // Do not leave while copies issued by this warp may still be landing.
     if (lane == 0) {
-      for (int grp = max(0, ngroups - Gm::kKGroups); grp < ngroups; ++grp)
-        mbar_wait(&ms.k_full[grp % Gm::kKGroups],
-                  static_cast<uint32_t>(grp / Gm::kKGroups) & 1u, p.timeout_ns);
-      for (int grp = max(0, ngroups - Gm::kVGroups); grp < ngroups; ++grp)
-        mbar_wait(&ms.v_full[grp % Gm::kVGroups],
-                  static_cast<uint32_t>(grp / Gm::kVGroups) & 1u, p.timeout_ns);
+      for (int grp = max(0, ngroups - ngr); grp < ngroups; ++grp)
+        mbar_wait(&fullb[grp % ngr], static_cast<uint32_t>(grp / ngr) & 1u, p.timeout_ns);
     }
   } else if (warp == Gm::kSoftmaxWarps + 1) {
     // ---------------------------------------------------------------- MMA issue
@@ -338,7 +331,6 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
                           static_cast<uint32_t>(pv / Gm::kVGroups) & 1u)) {
           tc::fence_after_sync();
           const int vb = pv % Gm::kVGroups;
-          const int pb = pv & 1;
           for (int j = 0; j < Gm::kGroupPages; ++j) {
             if (pv * Gm::kGroupPages + j >= npages || !ms.stage_ok[pv & 3][j]) continue;
             const int sl = vb * Gm::kGroupPages + j;
@@ -348,13 +340,13 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
                                               1024);
             // B = [P_hi^T | P_lo^T] (MN-major, no swizzle): this page's two token
             // blocks (leading offset), row-slot blocks kPNStride apart (stride offset)
-            const uint64_t bd = tc::smem_desc(psm + pb * Gm::kPBytes + j * 2 * Gm::kPKStride,
+            const uint64_t bd = tc::smem_desc(psm + j * 2 * Gm::kPKStride,
                                               Gm::kPKStride, Gm::kPNStride, tc::kSwizzleNone);
             tc::mma_f16_ss(tmem_o, ad, bd, kIdPV, any_pv);
             any_pv = 1u;
           }
           tc::commit(&ms.v_empty[vb]);
-          tc::commit(&ms.p_empty[pb]);
+          tc::commit(&ms.p_empty);
           ++pv;
           prog = true;
         }
@@ -372,7 +364,7 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
           }
           for (; pv < ngroups; ++pv) {
             mbar_arrive(&ms.v_empty[pv % Gm::kVGroups]);
-            mbar_arrive(&ms.p_empty[pv & 1]);
+            mbar_arrive(&ms.p_empty);
           }
         }
       }
@@ -390,12 +382,15 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const float sl2 = p.scale_log2;
     const int bar = 1 + hf;                    // named barrier of this half's 4 warps
-    float m[NH], lp[NH], thr[NH];
-    int lim[NH];
+    // per row slot: reference max m, the threshold m + 8 past which it moves,
+    // the exponent offset (m, or 0 while the row has seen nothing), row sum
+    float m[NA], thr[NA], mref[NA], lp[NA];
+    int lim[NA];
 #pragma unroll
-    for (int k = 0; k < NH; ++k) {
+    for (int k = 0; k < NA; ++k) {
       m[k] = -CUDART_INF_F;
       thr[k] = -CUDART_INF_F;
+      mref[k] = 0.f;
       lp[k] = 0.f;
       lim[k] = ms.lim[hf * NH + k];
     }
@@ -429,14 +424,21 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
                          static_cast<unsigned>(id) < static_cast<unsigned>(p.num_blocks);
       const int j = (pg0 + pidx) * kBlockSize + (t & 15);
       const bool interior = valid && nowin && j <= minlim;
-      float x[NH];
+      float x[NA];
       bool exceed = false;
+      if (interior) {                          // every row of the unit sees this token
 #pragma unroll
-      for (int k = 0; k < NH; ++k) {
-        const bool vis = k < cnt && (interior || (valid &&
-                         static_cast<unsigned>(lim[k] - j) < p.wcap));
-        x[k] = vis ? __uint_as_float(sr[k]) * sl2 : -CUDART_INF_F;
-        exceed |= x[k] > thr[k];
+        for (int k = 0; k < NA; ++k) {
+          x[k] = k < cnt ? __uint_as_float(sr[k]) * sl2 : -CUDART_INF_F;
+          exceed |= x[k] > thr[k];
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < NA; ++k) {
+          const bool vis = k < cnt && valid && static_cast<unsigned>(lim[k] - j) < p.wcap;
+          x[k] = vis ? __uint_as_float(sr[k]) * sl2 : -CUDART_INF_F;
+          exceed |= x[k] > thr[k];
+        }
       }
       // decision of this half on moving its rows' reference maxima
       // (bit 0: some score of the warp exceeds its row's threshold; bit 1: the
@@ -450,17 +452,17 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
       const bool any = (fl & 1) != 0;
       if (any) {
 #pragma unroll
-        for (int k = 0; k < NH; ++k) {
+        for (int k = 0; k < NA; ++k) {
           float v = x[k];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
           if (lane == 0) ms.red[hf][q][k] = v;
         }
         named_bar_sync(bar, 128);
-        float alpha[NH];
+        float alpha[NA];
         bool need_o = false;
 #pragma unroll
-        for (int k = 0; k < NH; ++k) {
+        for (int k = 0; k < NA; ++k) {
           const float mx = fmaxf(fmaxf(ms.red[hf][0][k], ms.red[hf][1][k]),
                                  fmaxf(ms.red[hf][2][k], ms.red[hf][3][k]));
           alpha[k] = 1.f;
@@ -473,16 +475,16 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
             }
             m[k] = mx;
             thr[k] = mx + 8.f;
+            mref[k] = mx;
           }
           lp[k] *= alpha[k];
         }
         named_bar_sync(bar, 128);              // red[] may be rewritten next group
         if (need_o && pv_before && !aborted) {
-          // O holds the pages of earlier groups: wait for their P.V (group grp - 1,
-          // whose buffer's previous P.V, of group grp - 3, this thread already
-          // waited for), then rescale this half's columns in TMEM
-          if (!mbar_wait(&ms.p_empty[(grp - 1) & 1], static_cast<uint32_t>((grp - 1) >> 1) & 1u,
-                         p.timeout_ns))
+          // O holds the pages of earlier groups: wait for their P.V (that of group
+          // grp - 1; this thread waited for the one before it), then rescale this
+          // half's columns in TMEM
+          if (!mbar_wait(&ms.p_empty, (static_cast<uint32_t>(grp) & 1u) ^ 1u, p.timeout_ns))
             aborted = true;
           aborted = __any_sync(0xffffffffu, aborted);
           tc::fence_after_sync();
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
           tc::tmem_ld16(tmem_o + lane_addr + NR + hf * NH, ol);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < NH; ++k) {
+          for (int k = 0; k < NA; ++k) {
             oh[k] = __float_as_uint(__uint_as_float(oh[k]) * alpha[k]);
             ol[k] = __float_as_uint(__uint_as_float(ol[k]) * alpha[k]);
           }
@@ -504,10 +506,10 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
       // of 8 row slots per token and core matrix)
       uint32_t hi[NH / 2], lo[NH / 2];
 #pragma unroll
-      for (int k = 0; k < NH; k += 2) {
-        const float m0 = m[k] == -CUDART_INF_F ? 0.f : m[k];
-        const float m1 = m[k + 1] == -CUDART_INF_F ? 0.f : m[k + 1];
-        const float p0 = hw_exp2(x[k] - m0), p1 = hw_exp2(x[k + 1] - m1);
+      for (int k = NA; k < NH; k += 2) hi[k / 2] = lo[k / 2] = 0u;
+#pragma unroll
+      for (int k = 0; k < NA; k += 2) {
+        const float p0 = hw_exp2(x[k] - mref[k]), p1 = hw_exp2(x[k + 1] - mref[k + 1]);
         lp[k] += p0;
         lp[k + 1] += p1;
         const uint32_t h2 = pack_bf16x2(p0, p1);
@@ -516,10 +518,11 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
                                 p1 - __uint_as_float(h2 & 0xFFFF0000u));
       }
       const int pb = grp & 1;
-      if (!aborted && !mbar_wait(&ms.p_empty[pb], (static_cast<uint32_t>(grp >> 1) & 1u) ^ 1u,
+      // the P operand is free once the P.V of group grp - 1 has completed
+      if (!aborted && !mbar_wait(&ms.p_empty, (static_cast<uint32_t>(grp) & 1u) ^ 1u,
                                  p.timeout_ns))
         aborted = true;
-      uint8_t* pt = smem + Gm::kPOff + pb * Gm::kPBytes + (t >> 3) * Gm::kPKStride + (t & 7) * 16;
+      uint8_t* pt = smem + Gm::kPOff + (t >> 3) * Gm::kPKStride + (t & 7) * 16;
 #pragma unroll
       for (int c = 0; c < NH / 8; ++c) {
         *reinterpret_cast<uint4*>(pt + (2 * hf + c) * Gm::kPNStride) =
@@ -553,10 +556,9 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
     }
 
     // ---------------------------------------------------------------- epilogue
-    // the last group's P.V (the one before it on the same buffer was waited for)
+    // the last group's P.V (this thread waited for the one before it)
     if (ngroups > 0 && !aborted &&
-        !mbar_wait(&ms.p_empty[(ngroups - 1) & 1], static_cast<uint32_t>((ngroups - 1) >> 1) & 1u,
-                   p.timeout_ns))
+        !mbar_wait(&ms.p_empty, static_cast<uint32_t>(ngroups - 1) & 1u, p.timeout_ns))
       aborted = true;
     aborted = __any_sync(0xffffffffu, aborted);
     tc::fence_after_sync();
@@ -565,7 +567,7 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
     tc::tmem_ld16(tmem_o + lane_addr + NR + hf * NH, ol);
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int k = 0; k < NH; ++k) {
+    for (int k = 0; k < NA; ++k) {
       float v = lp[k];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -573,15 +575,19 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
     }
     named_bar_sync(bar, 128);
     const int d = t;                           // head dim of this thread's O^T lane
+    const int r0 = hf == 0 ? 0 : hA;           // first query row of this half
+    int tq = r0 / G, hl = r0 % G;              // its draft token and head in the group
 #pragma unroll
-    for (int k = 0; k < NH; ++k) {
+    for (int k = 0; k < NA; ++k) {
       if (k >= cnt) break;
       const float Ls = ms.red[hf][0][k] + ms.red[hf][1][k] + ms.red[hf][2][k] + ms.red[hf][3][k];
-      const int r = hf == 0 ? k : hA + k;
-      const int tq = r / G, hl = r % G;
       const size_t orow = (static_cast<size_t>(b) * T + tq) * p.Hq + g * G + hl;
+      if (++hl == G) {
+        hl = 0;
+        ++tq;
+      }
       const float osum = __uint_as_float(oh[k]) + __uint_as_float(ol[k]);
-      const float o = Ls > 0.f ? osum / Ls : 0.f;
+      const float o = Ls > 0.f ? osum * __frcp_rn(Ls) : 0.f;
       if (direct) {
         reinterpret_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(o);
       } else {
@@ -602,10 +608,11 @@ __global__ void __launch_bounds__(TcGeo::kThreads, 1)
   }
 }
 
-inline cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                             dim3 grid, cudaStream_t s, bool overlap_previous) {
+template <int NA>
+cudaError_t launch_tc_na(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                         dim3 grid, cudaStream_t s, bool overlap_previous) {
   constexpr int smem = TcGeo::kAlloc;
-  auto kern = paged_attn_tc_kernel;
+  auto kern = paged_attn_tc_kernel<NA>;
   static std::atomic<unsigned long long> configured{0ull};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -627,6 +634,13 @@ inline cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+// rows = query rows per kv head (17 .. 32)
+inline cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                             int rows, dim3 grid, cudaStream_t s, bool overlap_previous) {
+  if (rows <= 20) return launch_tc_na<10>(tk, tv, p, grid, s, overlap_previous);
+  return launch_tc_na<16>(tk, tv, p, grid, s, overlap_previous);
 }
 
 }  // namespace pa

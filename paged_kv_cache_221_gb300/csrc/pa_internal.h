@@ -80,7 +80,7 @@ cudaError_t launch_attn_group8_d128(const CUtensorMap& tk, const CUtensorMap& tv
                                     const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
 // tcgen05 kernel (head_dim 128, bf16 pages, 17-32 query rows per kv head).
 cudaError_t launch_attn_tc_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                                dim3 grid, cudaStream_t s, bool overlap_previous);
+                                int rows, dim3 grid, cudaStream_t s, bool overlap_previous);
 cudaError_t launch_reshape_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
                                const int64_t* slots, const float* k_scale, const float* v_scale,
                                int num_tokens, int num_blocks, int hkv, int head_dim,
