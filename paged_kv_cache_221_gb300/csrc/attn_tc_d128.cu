@@ -6,7 +6,7 @@ namespace pa {
 
 cudaError_t launch_attn_tc_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                                 int rows, dim3 grid, cudaStream_t s, bool overlap_previous) {
-  return launch_tc(tk, tv, p, rows, grid, s, overlap_previous);
+  return launch_tc(tk, tv, p, rows, static_cast<int>(grid.x), s, overlap_previous);
 }
 
 cudaError_t take_error_attn_tc_d128(unsigned* bits) {

@@ -92,6 +92,7 @@ struct Plan {
   int max_parts = 1;     // partition slots per query row
   size_t ws_bytes = 0;   // scratch needed
   size_t off_ml = 0;
+  size_t off_counter = 0;  // work-unit counter of the tcgen05 kernel
 };
 
 // Partition sizes measured best on GB300: contexts up to 1024 tokens stay
@@ -114,7 +115,8 @@ int default_partition_tokens(int max_context_len, int num_seqs, int num_kv_heads
   return 2048;
 }
 
-// Scratch layout: [O partials][(m, l) pairs], each region 256-byte aligned.
+// Scratch layout: [O partials][(m, l) pairs][work-unit counter], each region
+// 256-byte aligned.
 Plan make_plan(int num_seqs, int hq, int T, int max_ctx, int head_dim, int partition_size,
                int max_prefix_blocks) {
   Plan pl;
@@ -128,7 +130,8 @@ Plan make_plan(int num_seqs, int hq, int T, int max_ctx, int head_dim, int parti
   const size_t po = round256(rows * pl.max_parts * head_dim * sizeof(float));
   const size_t pm = round256(rows * pl.max_parts * 2 * sizeof(float));
   pl.off_ml = po;
-  pl.ws_bytes = po + pm;
+  pl.off_counter = po + pm;
+  pl.ws_bytes = po + pm + 256;
   return pl;
 }
 
@@ -291,8 +294,15 @@ pa_status run_attention(const AttnArgs& a) {
     if (a.kv8)
       e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                            : launch_attn8_d128(tk, tv, p, rows, grid, a.stream, group_launch);
-    else if (a.head_dim == 128 && rows > 16 && rows <= 32 && tensor_core_kernel_enabled())
+    else if (a.head_dim == 128 && rows > 16 && rows <= 32 && tensor_core_kernel_enabled()) {
+      // With scratch, the persistent CTAs claim units from a counter zeroed here.
+      if (plan.ws_bytes > 0) {
+        p.unit_counter = reinterpret_cast<int*>(static_cast<char*>(a.workspace) + plan.off_counter);
+        e = cudaMemsetAsync(p.unit_counter, 0, sizeof(int), a.stream);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+      }
       e = launch_attn_tc_d128(tk, tv, p, rows, grid, a.stream, group_launch);
+    }
     else
       e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                            : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);

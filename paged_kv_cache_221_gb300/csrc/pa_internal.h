@@ -49,6 +49,8 @@ struct AttnParams {
   int wspan;                      // window, or 2^30 without one (interior pages: tok0 +
                                   //   wspan >= context length)
   unsigned long long timeout_ns;  // limit of every pipeline wait
+  int* unit_counter;              // tcgen05 kernel: next work unit to claim (zeroed before the
+                                  //   launch), or nullptr for a fixed round-robin order
 };
 
 // Split-KV scratch bytes a call with these sizes needs (partition_size 0 = the

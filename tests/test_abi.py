@@ -48,8 +48,8 @@ def test_workspace_size_host_only(lib):
     def r256(x):
         return (x + 255) // 256 * 256
 
-    def want(slots):        # [O partials][(m, l) pairs]
-        return r256(rows * slots * 128 * 4) + r256(rows * slots * 8)
+    def want(slots):        # [O partials][(m, l) pairs][256-B work-unit counter]
+        return r256(rows * slots * 128 * 4) + r256(rows * slots * 8) + 256
 
     assert lib.pa_workspace_size(64, 32, 1, 4096, 128, 16, 512, 0) == want(8)
     # default: the largest need over kv-head counts; one kv head (64 pairs, a small
