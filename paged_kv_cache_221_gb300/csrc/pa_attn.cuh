@@ -49,12 +49,16 @@ namespace pa {
 template <int D, bool KV8 = false>
 struct Geo {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
-  static constexpr int kNS = KV8 ? 2 * kStages : kStages;   // ring stages (same ring bytes)
-  static constexpr int kIssueGroup = KV8 ? 8 : 4;            // pages the producer issues at once
+  // A ring stage holds kPPS consecutive pages of the unit: their K pages, then
+  // their V pages.  FP8 pages are half the bytes of bf16 pages, so a stage holds
+  // two of them and the ring moves the same bytes per barrier round trip.
+  static constexpr int kPPS = KV8 ? 2 : 1;              // pages per ring stage
+  static constexpr int kNS = kStages;                   // ring stages
+  static constexpr int kIssueGroup = 4;                 // stages the producer issues at once
   static constexpr int kHalves = D / 64;                // bf16: 128-byte swizzle rows per token
   static constexpr int kHalfBytes = kBlockSize * 128;   // bf16: one 16 x 64 TMA box
   static constexpr int kPageBytes = kBlockSize * D * (KV8 ? 1 : 2);
-  static constexpr int kStageBytes = 2 * kPageBytes;    // K page + V page
+  static constexpr int kStageBytes = 2 * kPPS * kPageBytes;
   static constexpr int kQStride = D + 8;                // bf16 per Q row in smem (conflict-free)
   static constexpr int kOStride = D + 4;                // floats per merge row (conflict-free)
   static constexpr int kKSteps = D / 16;
@@ -63,8 +67,9 @@ struct Geo {
 // Consumer-warp layout: NT n-tiles of 8 query rows per warp, NTW warp columns
 // (rows 8*NT*NTW per CTA), PL page lanes (warps of one column that split the
 // pages), and the CTAs per SM the register budget must allow.
-// TP: pages per softmax step of a consumer warp (2 needs at least four ring
-// stages per page lane: two in use, two in flight).
+// TP: ring stages per softmax step of a consumer warp (2 needs at least four
+// ring stages per page lane: two in use, two in flight).  FP8 pages take one
+// stage (two pages) per step whatever TP says.
 template <int NT_, int NTW_, int PL_, int MINB_, int TP_ = 1>
 struct Cfg {
   static constexpr int NT = NT_, NTW = NTW_, PL = PL_, MINB = MINB_, TP = TP_;
@@ -125,10 +130,13 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   using Gm = Geo<D, KV8>;
   using Sm = Smem<D, NT, NTW, KV8>;
   constexpr int NS = Gm::kNS;
+  constexpr int PPS = Gm::kPPS;              // pages per ring stage
+  constexpr int TPI = KV8 ? 1 : C::TP;       // ring stages per consumer step
+  constexpr int TP = TPI * PPS;              // pages per consumer step
   static_assert(NS % PL == 0, "each stage is always consumed by the same page lane");
   static_assert(PL * NTW * Sm::kMergeFloats * 4 <= NS * Gm::kStageBytes,
                 "merge buffers fit in the stage ring");
-  static_assert(C::TP == 1 || NS / PL >= 4, "ring too short for two pages per step");
+  static_assert(TPI == 1 || NS / PL >= 4, "ring too short for two stages per step");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -238,6 +246,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 
   // ------------------------------------------------------------------ setup
   const int npages = pg1 - pg0;
+  const int nitems = (npages + PPS - 1) / PPS;   // ring stages the unit fills
   const int32_t* trow =
       p.block_tables + static_cast<size_t>(GROUP ? members[0] : b_single) * p.mbs;
   int phys_first = 0;                        // first 32 block ids, loaded before the sync
@@ -259,12 +268,13 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 
   // ------------------------------------------------------------------ producer
   // Starts streaming pages at once; the consumers gather the query rows meanwhile.
-  // Pages are issued in groups of GP: lane j of the group waits for its own
-  // stage and issues its own page, so one pass of the loop puts GP pages in
-  // flight (the per-page cost of waiting and issuing is paid once per group).
+  // Stages are issued in groups of GP: lane j of the group waits for its own
+  // stage and issues its own page(s), so one pass of the loop puts GP stages in
+  // flight (the per-stage cost of waiting and issuing is paid once per group).
   if (warp == NCW) {
     constexpr int GP = Gm::kIssueGroup;
-    static_assert(GP >= 1 && GP <= NS && 32 % GP == 0, "issue group");
+    constexpr int IPB = 32 / PPS;             // stages per batch of 32 block ids
+    static_assert(GP >= 1 && GP <= NS && IPB % GP == 0, "issue group");
     bool aborted = false;
     // Query tokens' K/V that land in this unit's pages are stored into the pool
     // first (reshape_and_cache fused; FP8 pages quantise on the way).  The stores
@@ -334,39 +344,57 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       __syncwarp();
       pending = false;
     };
-    if (pending && jlo < GP) store_new_tokens();   // the first group holds a new token
+    if (pending && jlo < GP * PPS) store_new_tokens();   // the first group holds a new token
     for (int base = 0; base < npages; base += 32) {
       const int phys_l = base == 0 ? phys_first
                                    : ((base + lane < npages) ? __ldg(trow + pg0 + base + lane) : 0);
       const int cnt = min(32, npages - base);
-      for (int j0 = 0; j0 < cnt; j0 += GP) {
-        const int jn = min(j0 + GP, cnt);
-        if (base + jn > fence_at) {
+      const int icnt = (cnt + PPS - 1) / PPS;   // stages of this batch
+      // lane i takes pages base + PPS*i .. base + PPS*i + PPS - 1 (lanes below IPB)
+      int phys_a = phys_l, phys_b = 0;
+      if constexpr (PPS == 2) {
+        phys_a = __shfl_sync(0xffffffffu, phys_l, (2 * lane) & 31);
+        phys_b = __shfl_sync(0xffffffffu, phys_l, (2 * lane + 1) & 31);
+      }
+      for (int j0 = 0; j0 < icnt; j0 += GP) {
+        const int jn = min(j0 + GP, icnt);
+        if (min(npages, base + PPS * jn) > fence_at) {
           // the stores must be visible to the TMA reads of the pages that hold them
           fence_proxy_async_global();
           __syncwarp();
           fence_at = npages;
         }
         if (lane >= j0 && lane < jn) {
-          const int it = base + lane;
+          const int it = base / PPS + lane;
           const int s = it % NS;
           const uint32_t ph = static_cast<uint32_t>(it / NS) & 1u;
           if (!aborted && !mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns)) aborted = true;
-          const bool ok = static_cast<unsigned>(phys_l) < static_cast<unsigned>(p.num_blocks);
+          const bool two = PPS == 2 && base + 2 * lane + 1 < npages;
+          const bool ok = static_cast<unsigned>(phys_a) < static_cast<unsigned>(p.num_blocks) &&
+                          (!two || static_cast<unsigned>(phys_b) <
+                                       static_cast<unsigned>(p.num_blocks));
           if (!ok) atomicOr(&g_pa_err, kErrBounds);
           if (!ok || aborted) {
             stage_ok[s] = 0;
             mbar_arrive(&full[s]);
           } else {
             stage_ok[s] = 1;
-            mbar_arrive_expect_tx(&full[s], Gm::kStageBytes);
-            const int row = (phys_l * p.Hkv + g) * kBlockSize;
             uint8_t* st = stages + s * Gm::kStageBytes;
             if constexpr (KV8) {
-              tma_load_2d(st, &tmk, &full[s], 0, row);                      // 16 x D codes
-              tma_load_2d(st + Gm::kPageBytes, &tmv, &full[s], 0,
-                          (phys_l * p.Hkv + g) * (D / 8));                   // D x 16 codes
+              // K pages at 0 and kPageBytes, V pages at 2 and 3 kPageBytes
+              mbar_arrive_expect_tx(&full[s], (two ? 4 : 2) * Gm::kPageBytes);
+              tma_load_2d(st, &tmk, &full[s], 0, (phys_a * p.Hkv + g) * kBlockSize);
+              tma_load_2d(st + 2 * Gm::kPageBytes, &tmv, &full[s], 0,
+                          (phys_a * p.Hkv + g) * (D / 8));
+              if (two) {
+                tma_load_2d(st + Gm::kPageBytes, &tmk, &full[s], 0,
+                            (phys_b * p.Hkv + g) * kBlockSize);
+                tma_load_2d(st + 3 * Gm::kPageBytes, &tmv, &full[s], 0,
+                            (phys_b * p.Hkv + g) * (D / 8));
+              }
             } else {
+              mbar_arrive_expect_tx(&full[s], Gm::kStageBytes);
+              const int row = (phys_a * p.Hkv + g) * kBlockSize;
 #pragma unroll
               for (int h = 0; h < Gm::kHalves; ++h)
                 tma_load_2d(st + h * Gm::kHalfBytes, &tmk, &full[s], h * 64, row);
@@ -384,7 +412,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     }
     // Do not leave while copies issued by this warp may still be landing.
     if (lane == 0) {
-      for (int it = max(0, npages - NS); it < npages; ++it)
+      for (int it = max(0, nitems - NS); it < nitems; ++it)
         mbar_wait(&full[it % NS], static_cast<uint32_t>(it / NS) & 1u, p.timeout_ns);
     }
     return;
@@ -509,30 +537,40 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   for (int j = 0; j < NT; ++j) minlim = min(minlim, min(lim0[j], lim1[j]));
   minlim = __reduce_min_sync(0xffffffffu, minlim);
 
-  // Each step handles TP pages of this lane (it, it + PL, ...): one score tile
-  // per page, one softmax update over all of them, one P.V per page.
-  constexpr int TP = C::TP;
-  for (int it = pl; it < npages; it += TP * PL) {
+  // Each step handles TPI stages of this lane (it, it + PL, ...), TP pages in
+  // all: one score tile per page, one softmax update over all of them, one P.V
+  // per page.
+  for (int it = pl; it < nitems; it += TPI * PL) {
     int nstep = 1;
-    if (TP == 2 && it + PL < npages) nstep = 2;
+    if (TPI == 2 && it + PL < nitems) nstep = 2;
     bool okp[TP];
     uint32_t kb[TP], vb[TP];
-    int tok0[TP], sidx[TP];
+    int tok0[TP], sidx[TPI];
 #pragma unroll
     for (int k = 0; k < TP; ++k) {
       okp[k] = false;
       kb[k] = vb[k] = 0;
-      tok0[k] = sidx[k] = 0;
-      if (k < nstep) {
-        const int pg = it + k * PL;
-        const int s = pg % NS;
-        const uint32_t ph = static_cast<uint32_t>(pg / NS) & 1u;
+      tok0[k] = 0;
+    }
+#pragma unroll
+    for (int si = 0; si < TPI; ++si) {
+      sidx[si] = 0;
+      if (si < nstep) {
+        const int item = it + si * PL;
+        const int s = item % NS;
+        const uint32_t ph = static_cast<uint32_t>(item / NS) & 1u;
         if (!aborted && !mbar_wait(&full[s], ph, p.timeout_ns)) aborted = true;
-        okp[k] = !aborted && stage_ok[s];
-        sidx[k] = s;
-        kb[k] = smem_u32(stages + s * Gm::kStageBytes);
-        vb[k] = kb[k] + Gm::kPageBytes;
-        tok0[k] = (pg0 + pg) * kBlockSize;
+        const bool ok = !aborted && stage_ok[s];
+        sidx[si] = s;
+        const uint32_t sb = smem_u32(stages + s * Gm::kStageBytes);
+#pragma unroll
+        for (int u = 0; u < PPS; ++u) {
+          const int k = si * PPS + u, pg = item * PPS + u;
+          okp[k] = ok && pg < npages;
+          kb[k] = sb + u * Gm::kPageBytes;
+          vb[k] = sb + (PPS + u) * Gm::kPageBytes;
+          tok0[k] = (pg0 + pg) * kBlockSize;
+        }
       }
     }
 
@@ -757,8 +795,8 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     __syncwarp();
     if (lane == 0) {
 #pragma unroll
-      for (int k = 0; k < TP; ++k)
-        if (k < nstep) mbar_arrive(&empty[sidx[k]]);
+      for (int si = 0; si < TPI; ++si)
+        if (si < nstep) mbar_arrive(&empty[sidx[si]]);
     }
   }
 
