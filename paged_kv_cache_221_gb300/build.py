@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(HERE, "libpaged_attn.so")
 
 SOURCES = ["pa_api.cpp", "pa_misc.cu", "attn_d64.cu", "attn_d128.cu", "group_d64.cu",
            "group_d128.cu", "attn8_d64.cu", "attn8_d128.cu", "group8_d64.cu", "group8_d128.cu",
-           "pa_spec.cu", "pa_no_alloc.cu", "attn_tc_d128.cu",
+           "pa_spec.cu", "pa_no_alloc.cu", "attn_tc_d128.cu", "stream_d64.cu", "stream_d128.cu",
            "pa_runner.cpp", "pa_block_manager.cpp"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE,

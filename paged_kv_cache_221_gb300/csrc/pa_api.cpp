@@ -83,6 +83,18 @@ bool tensor_core_kernel_enabled() {
   return v != nullptr && std::strcmp(v, "tcgen05") == 0;
 }
 
+// Kernel for at most 8 query rows per kv head: the environment variable
+// PA_DECODE_KERNEL = "per_unit" selects the one-CTA-per-unit kernel,
+// "persistent" the persistent kernel; unset (or anything else), the library
+// chooses (read on every call, so that a process can compare them).
+enum StreamMode { kStreamNever = 0, kStreamAuto = 1, kStreamAlways = 2 };
+StreamMode stream_kernel_mode() {
+  const char* v = std::getenv("PA_DECODE_KERNEL");
+  if (v != nullptr && std::strcmp(v, "per_unit") == 0) return kStreamNever;
+  if (v != nullptr && std::strcmp(v, "persistent") == 0) return kStreamAlways;
+  return kStreamAuto;
+}
+
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -291,26 +303,50 @@ pa_status run_attention(const AttnArgs& a) {
                             a.num_seqs;
     if (units >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(units), 1, 1);
-    if (a.kv8)
-      e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream, group_launch)
-                           : launch_attn8_d128(tk, tv, p, rows, grid, a.stream, group_launch);
-    else if (a.head_dim == 128 && rows > 16 && rows <= 32 && tensor_core_kernel_enabled()) {
-      // With scratch, the persistent CTAs claim units from a counter zeroed here.
-      if (plan.ws_bytes > 0) {
-        p.unit_counter = reinterpret_cast<int*>(static_cast<char*>(a.workspace) + plan.off_counter);
-        e = cudaMemsetAsync(p.unit_counter, 0, sizeof(int), a.stream);
-        if (e != cudaSuccess) return PA_ERR_CUDA;
-      }
-      e = launch_attn_tc_d128(tk, tv, p, rows, grid, a.stream, group_launch);
+    const StreamMode mode = stream_kernel_mode();
+    bool launched = false;
+    if (!grouped && rows <= 8 && a.num_seqs <= kStreamMaxSeqs && plan.ppb <= kStreamMaxPpb &&
+        mode != kStreamNever) {
+      // Claim state 16 bytes into the counter area (the tcgen05 kernel's
+      // counter is the first 4 bytes).
+      if (plan.ws_bytes > 0)
+        p.stream_ctl = static_cast<char*>(a.workspace) + plan.off_counter + 16;
+      const bool always = mode == kStreamAlways;
+      e = a.head_dim == 64
+              ? launch_stream_d64(tk, tv, p, rows, units, a.kv8, always, a.stream, &launched)
+              : launch_stream_d128(tk, tv, p, rows, units, a.kv8, always, a.stream, &launched);
+      if (e != cudaSuccess) return PA_ERR_CUDA;
+      if (!launched) p.stream_ctl = nullptr;
     }
-    else
-      e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
-                           : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (!launched) {
+      if (a.kv8) {
+        e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream, group_launch)
+                             : launch_attn8_d128(tk, tv, p, rows, grid, a.stream, group_launch);
+      } else if (a.head_dim == 128 && rows > 16 && rows <= 32 && tensor_core_kernel_enabled()) {
+        // With scratch, the persistent CTAs claim units from a counter zeroed here.
+        if (plan.ws_bytes > 0) {
+          p.unit_counter =
+              reinterpret_cast<int*>(static_cast<char*>(a.workspace) + plan.off_counter);
+          e = cudaMemsetAsync(p.unit_counter, 0, sizeof(int), a.stream);
+          if (e != cudaSuccess) return PA_ERR_CUDA;
+        }
+        e = launch_attn_tc_d128(tk, tv, p, rows, grid, a.stream, group_launch);
+      } else {
+        e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
+                             : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);
+      }
+      if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
   }
   if (plan.ws_bytes > 0) {
     e = launch_reduce(p, a.head_dim, a.stream);
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (e != cudaSuccess) {
+      // The merge resets the persistent kernel's claim counter; without it the
+      // tag must go, so that the next launch on this scratch does not claim
+      // from a stale counter.
+      if (p.stream_ctl != nullptr) cudaMemsetAsync(p.stream_ctl, 0, sizeof(StreamCtl), a.stream);
+      return PA_ERR_CUDA;
+    }
   }
   return PA_OK;
 }
@@ -603,7 +639,8 @@ pa_status pa_get_device_error(pa_stream_t stream) {
       take_error_group_d128(&bits) != cudaSuccess || take_error_attn8_d64(&bits) != cudaSuccess ||
       take_error_attn8_d128(&bits) != cudaSuccess || take_error_group8_d64(&bits) != cudaSuccess ||
       take_error_group8_d128(&bits) != cudaSuccess || take_error_spec(&bits) != cudaSuccess ||
-      take_error_attn_tc_d128(&bits) != cudaSuccess || take_error_misc(&bits) != cudaSuccess)
+      take_error_attn_tc_d128(&bits) != cudaSuccess || take_error_stream_d64(&bits) != cudaSuccess ||
+      take_error_stream_d128(&bits) != cudaSuccess || take_error_misc(&bits) != cudaSuccess)
     return PA_ERR_CUDA;
   if (bits & kErrTimeout) return PA_ERR_TIMEOUT;
   if (bits & kErrBounds) return PA_ERR_BOUNDS;

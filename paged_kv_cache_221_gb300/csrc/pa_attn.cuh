@@ -120,6 +120,250 @@ __device__ __forceinline__ int sigma_row(int m) {
   return 4 * ((m & 7) >> 1) + (m & 1) + 2 * (m >> 3);
 }
 
+// One consumer step: the score tiles of TP staged pages (K_page . Q^T per page
+// and n-tile), one online-softmax update of the warp's rows over all of them,
+// and the P.V accumulation of every page into the output tile.  okp[k] false
+// means page k is absent (its scores are -inf, it adds nothing).
+template <int D, int NT, int TP, bool KV8>
+struct StepState {
+  float acc[NT][D / 16][4];
+  float m0[NT], m1[NT], l0[NT], l1[NT];
+};
+
+template <int D, int NT, int TP, bool KV8, bool kQRegs>
+__device__ __forceinline__ void attend_step(
+    StepState<D, NT, TP, KV8>& st, const bool (&okp)[TP], const uint32_t (&kb)[TP],
+    const uint32_t (&vb)[TP], const int (&tok0)[TP],
+    const uint32_t (&qf)[kQRegs ? NT : 1][kQRegs ? D / 16 : 1][2], uint32_t qrow,
+    const uint32_t (&koff)[4], const uint32_t (&voff)[4], const int (&lim0)[NT],
+    const int (&lim1)[NT], int minlim, int vlen, float sl2, int srow0, int srow1, int q4,
+    const AttnParams& p) {
+  using Gm = Geo<D, KV8>;
+  auto& acc = st.acc;
+  auto& m0 = st.m0;
+  auto& m1 = st.m1;
+  auto& l0 = st.l0;
+  auto& l1 = st.l1;
+  // S^T[16 tokens x 8 rows] = K_page . Q^T per page and n-tile (two chains each)
+  float sa[TP][NT][4], sb[TP][NT][4];
+#pragma unroll
+  for (int k = 0; k < TP; ++k)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sa[k][j][e] = sb[k][j][e] = 0.f;
+#pragma unroll
+  for (int k = 0; k < TP; ++k) {
+    if (!okp[k]) continue;
+    if constexpr (KV8) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(r0, r1, r2, r3, kb[k] + koff[c]);
+        const uint32_t a00 = e4m3x2_to_f16x2(r0), a02 = e4m3x2_to_f16x2(r0 >> 16);
+        const uint32_t a01 = e4m3x2_to_f16x2(r1), a03 = e4m3x2_to_f16x2(r1 >> 16);
+        const uint32_t a10 = e4m3x2_to_f16x2(r2), a12 = e4m3x2_to_f16x2(r2 >> 16);
+        const uint32_t a11 = e4m3x2_to_f16x2(r3), a13 = e4m3x2_to_f16x2(r3 >> 16);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          uint32_t b00, b01, b10, b11;
+          if constexpr (kQRegs) {
+            b00 = qf[j][2 * c][0];
+            b01 = qf[j][2 * c][1];
+            b10 = qf[j][2 * c + 1][0];
+            b11 = qf[j][2 * c + 1][1];
+          } else {
+            ldsm_x4(b00, b01, b10, b11,
+                    qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + 2 * c * 32));
+          }
+          mma_f16_16816(sa[k][j], a00, a01, a02, a03, b00, b01);
+          mma_f16_16816(sb[k][j], a10, a11, a12, a13, b10, b11);
+        }
+      }
+    } else {
+#pragma unroll
+    for (int k2 = 0; k2 < Gm::kKSteps; k2 += 2) {
+      uint32_t a[2][4];
+      ldsm_x4(a[0][0], a[0][1], a[0][2], a[0][3],
+              kb[k] + (k2 >> 2) * Gm::kHalfBytes + koff[k2 & 3]);
+      ldsm_x4(a[1][0], a[1][1], a[1][2], a[1][3],
+              kb[k] + ((k2 + 1) >> 2) * Gm::kHalfBytes + koff[(k2 + 1) & 3]);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        uint32_t b00, b01, b10, b11;
+        if constexpr (kQRegs) {
+          b00 = qf[j][k2][0];
+          b01 = qf[j][k2][1];
+          b10 = qf[j][k2 + 1][0];
+          b11 = qf[j][k2 + 1][1];
+        } else {
+          ldsm_x4(b00, b01, b10, b11,
+                  qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + k2 * 32));
+        }
+        mma_bf16_16816(sa[k][j], a[0][0], a[0][1], a[0][2], a[0][3], b00, b01);
+        mma_bf16_16816(sb[k][j], a[1][0], a[1][1], a[1][2], a[1][3], b10, b11);
+      }
+    }
+    }
+  }
+
+  // V rows at or past the context end may hold anything (even NaN): their
+  // weight is 0, but 0 * NaN is NaN, so zero them in the operand.
+  int nvalid[TP];
+  bool interior[TP];
+  uint32_t mlo[TP], mhi[TP];
+#pragma unroll
+  for (int k = 0; k < TP; ++k) {
+    nvalid[k] = vlen - tok0[k];
+    interior[k] = okp[k] && (tok0[k] + kBlockSize - 1 <= minlim) &&
+                  (tok0[k] + p.wspan >= vlen) && (nvalid[k] >= kBlockSize);
+    mlo[k] = mhi[k] = 0xffffffffu;
+    if (nvalid[k] < kBlockSize) {
+      const int nv = nvalid[k];
+      // tokens behind the low / high halves of the first and second A register pairs
+      const int t0 = KV8 ? 4 * q4 : 2 * q4, t2 = KV8 ? 4 * q4 + 2 : 2 * q4 + 8;
+      mlo[k] = (t0 < nv ? 0x0000ffffu : 0u) | (t0 + 1 < nv ? 0xffff0000u : 0u);
+      mhi[k] = (t2 < nv ? 0x0000ffffu : 0u) | (t2 + 1 < nv ? 0xffff0000u : 0u);
+    }
+  }
+
+  uint32_t bh0[TP][NT], bh1[TP][NT], bl0[TP][NT], bl1[TP][NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    // lane holds S^T[j0][n], S^T[j0][n+1], S^T[j0+8][n], S^T[j0+8][n+1] of each
+    // page, n = rbase + 8j + 2q4 (t[k][0..3] in that order)
+    float t[TP][4];
+    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+    for (int k = 0; k < TP; ++k) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t[k][e] = (sa[k][j][e] + sb[k][j][e]) * sl2;
+      if (!okp[k]) {
+        t[k][0] = t[k][1] = t[k][2] = t[k][3] = -CUDART_INF_F;
+      } else if (!interior[k]) {
+        const int j0 = tok0[k] + srow0, j1 = tok0[k] + srow1;
+        const unsigned u0 = static_cast<unsigned>(j0), u1 = static_cast<unsigned>(j1);
+        t[k][0] = (static_cast<unsigned>(lim0[j]) - u0 < p.wcap) ? t[k][0] : -CUDART_INF_F;
+        t[k][1] = (static_cast<unsigned>(lim1[j]) - u0 < p.wcap) ? t[k][1] : -CUDART_INF_F;
+        t[k][2] = (static_cast<unsigned>(lim0[j]) - u1 < p.wcap) ? t[k][2] : -CUDART_INF_F;
+        t[k][3] = (static_cast<unsigned>(lim1[j]) - u1 < p.wcap) ? t[k][3] : -CUDART_INF_F;
+      }
+      mx0 = fmaxf(mx0, fmaxf(t[k][0], t[k][2]));
+      mx1 = fmaxf(mx1, fmaxf(t[k][1], t[k][3]));
+    }
+
+    // online softmax (log2 domain), statistics per row.  The reference max m
+    // only moves when a score exceeds it by more than 8 (so every weight
+    // 2^(t - m) stays <= 256); the accumulators are rescaled only then.
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const bool up0 = mx0 > m0[j] + 8.f, up1 = mx1 > m1[j] + 8.f;
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+      const float al0 = up0 ? hw_exp2(m0[j] - mx0) : 1.f;
+      const float al1 = up1 ? hw_exp2(m1[j] - mx1) : 1.f;
+      if (up0) m0[j] = mx0;
+      if (up1) m1[j] = mx1;
+      l0[j] *= al0;
+      l1[j] *= al1;
+#pragma unroll
+      for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+        acc[j][mt][0] *= al0;
+        acc[j][mt][1] *= al1;
+        acc[j][mt][2] *= al0;
+        acc[j][mt][3] *= al1;
+      }
+    }
+    const float mu0 = (m0[j] == -CUDART_INF_F) ? 0.f : m0[j];
+    const float mu1 = (m1[j] == -CUDART_INF_F) ? 0.f : m1[j];
+#pragma unroll
+    for (int k = 0; k < TP; ++k) {
+      const float p0 = hw_exp2(t[k][0] - mu0), p1 = hw_exp2(t[k][1] - mu1);
+      const float p2 = hw_exp2(t[k][2] - mu0), p3 = hw_exp2(t[k][3] - mu1);
+      l0[j] += p0 + p2;
+      l1[j] += p1 + p3;
+      if constexpr (KV8) {
+        // P^T as one f16 B operand (transposed 8x8 blocks)
+        bh0[k][j] = movmatrix_trans(half2_bits(__floats2half2_rn(p0, p1)));
+        bh1[k][j] = movmatrix_trans(half2_bits(__floats2half2_rn(p2, p3)));
+        continue;
+      }
+      // P^T as B operands: bf16 high part and bf16 residual, transposed 8x8 blocks
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+      const float2 f01 = __bfloat1622float2(h01);
+      const float2 f23 = __bfloat1622float2(h23);
+      const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+      const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+      bh0[k][j] = movmatrix_trans(bf162_bits(h01));
+      bh1[k][j] = movmatrix_trans(bf162_bits(h23));
+      bl0[k][j] = movmatrix_trans(bf162_bits(r01));
+      bl1[k][j] = movmatrix_trans(bf162_bits(r23));
+    }
+  }
+
+  // O^T[D x 8] += V_page^T . P^T per page and n-tile
+#pragma unroll
+  for (int k = 0; k < TP; ++k) {
+    if (!okp[k]) continue;
+    auto pv = [&](auto tail) {
+      if constexpr (KV8) {
+        // transposed V: rows are head dims; ldmatrix c covers dims 32c .. 32c+31
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(r0, r1, r2, r3, vb[k] + voff[c]);
+          uint32_t a[2][4];
+          a[0][0] = e4m3x2_to_f16x2(r0);
+          a[0][2] = e4m3x2_to_f16x2(r0 >> 16);
+          a[0][1] = e4m3x2_to_f16x2(r1);
+          a[0][3] = e4m3x2_to_f16x2(r1 >> 16);
+          a[1][0] = e4m3x2_to_f16x2(r2);
+          a[1][2] = e4m3x2_to_f16x2(r2 >> 16);
+          a[1][1] = e4m3x2_to_f16x2(r3);
+          a[1][3] = e4m3x2_to_f16x2(r3 >> 16);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if constexpr (decltype(tail)::value) {
+              a[h][0] &= mlo[k];
+              a[h][1] &= mlo[k];
+              a[h][2] &= mhi[k];
+              a[h][3] &= mhi[k];
+            }
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+              mma_f16_16816(acc[j][2 * c + h], a[h][0], a[h][1], a[h][2], a[h][3],
+                            bh0[k][j], bh1[k][j]);
+          }
+        }
+      } else {
+#pragma unroll
+      for (int mt = 0; mt < Gm::kKSteps; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(a0, a1, a2, a3, vb[k] + (mt >> 2) * Gm::kHalfBytes + voff[mt & 3]);
+        if constexpr (decltype(tail)::value) {
+          a0 &= mlo[k];
+          a1 &= mlo[k];
+          a2 &= mhi[k];
+          a3 &= mhi[k];
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bh0[k][j], bh1[k][j]);
+          mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bl0[k][j], bl1[k][j]);
+        }
+      }
+      }
+    };
+    if (nvalid[k] < kBlockSize)
+      pv(std::true_type{});
+    else
+      pv(std::false_type{});
+  }
+}
+
 template <int D, class C, bool GROUP, bool KV8>
 __global__ void __launch_bounds__(C::kThreads, C::MINB)
     paged_attn_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -452,7 +696,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       int lm = 0x7fffffff;
       if (n < nrows) {
         const int m = n / (G * T), t = (n / G) % T;
-        lm = p.context_lens[GROUP ? members[m] : b_single] - T + t;
+        lm = (GROUP ? p.context_lens[members[m]] : vlen) - T + t;
       }
       lim[n] = lm;
     }
@@ -495,8 +739,12 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
                 qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + ks * 32));
   }
 
-  float acc[NT][Gm::kKSteps][4];
-  float m0[NT], m1[NT], l0[NT], l1[NT];
+  StepState<D, NT, TP, KV8> st;
+  auto& acc = st.acc;
+  auto& m0 = st.m0;
+  auto& m1 = st.m1;
+  auto& l0 = st.l0;
+  auto& l1 = st.l1;
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
 #pragma unroll
@@ -574,224 +822,8 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       }
     }
 
-    // S^T[16 tokens x 8 rows] = K_page . Q^T per page and n-tile (two chains each)
-    float sa[TP][NT][4], sb[TP][NT][4];
-#pragma unroll
-    for (int k = 0; k < TP; ++k)
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sa[k][j][e] = sb[k][j][e] = 0.f;
-#pragma unroll
-    for (int k = 0; k < TP; ++k) {
-      if (!okp[k]) continue;
-      if constexpr (KV8) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4(r0, r1, r2, r3, kb[k] + koff[c]);
-          const uint32_t a00 = e4m3x2_to_f16x2(r0), a02 = e4m3x2_to_f16x2(r0 >> 16);
-          const uint32_t a01 = e4m3x2_to_f16x2(r1), a03 = e4m3x2_to_f16x2(r1 >> 16);
-          const uint32_t a10 = e4m3x2_to_f16x2(r2), a12 = e4m3x2_to_f16x2(r2 >> 16);
-          const uint32_t a11 = e4m3x2_to_f16x2(r3), a13 = e4m3x2_to_f16x2(r3 >> 16);
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            uint32_t b00, b01, b10, b11;
-            if constexpr (kQRegs) {
-              b00 = qf[j][2 * c][0];
-              b01 = qf[j][2 * c][1];
-              b10 = qf[j][2 * c + 1][0];
-              b11 = qf[j][2 * c + 1][1];
-            } else {
-              ldsm_x4(b00, b01, b10, b11,
-                      qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + 2 * c * 32));
-            }
-            mma_f16_16816(sa[k][j], a00, a01, a02, a03, b00, b01);
-            mma_f16_16816(sb[k][j], a10, a11, a12, a13, b10, b11);
-          }
-        }
-        continue;
-      }
-#pragma unroll
-      for (int k2 = 0; k2 < Gm::kKSteps; k2 += 2) {
-        uint32_t a[2][4];
-        ldsm_x4(a[0][0], a[0][1], a[0][2], a[0][3],
-                kb[k] + (k2 >> 2) * Gm::kHalfBytes + koff[k2 & 3]);
-        ldsm_x4(a[1][0], a[1][1], a[1][2], a[1][3],
-                kb[k] + ((k2 + 1) >> 2) * Gm::kHalfBytes + koff[(k2 + 1) & 3]);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          uint32_t b00, b01, b10, b11;
-          if constexpr (kQRegs) {
-            b00 = qf[j][k2][0];
-            b01 = qf[j][k2][1];
-            b10 = qf[j][k2 + 1][0];
-            b11 = qf[j][k2 + 1][1];
-          } else {
-            ldsm_x4(b00, b01, b10, b11,
-                    qrow + static_cast<uint32_t>(j * 8 * Gm::kQStride * 2 + k2 * 32));
-          }
-          mma_bf16_16816(sa[k][j], a[0][0], a[0][1], a[0][2], a[0][3], b00, b01);
-          mma_bf16_16816(sb[k][j], a[1][0], a[1][1], a[1][2], a[1][3], b10, b11);
-        }
-      }
-    }
-
-    // V rows at or past the context end may hold anything (even NaN): their
-    // weight is 0, but 0 * NaN is NaN, so zero them in the operand.
-    int nvalid[TP];
-    bool interior[TP];
-    uint32_t mlo[TP], mhi[TP];
-#pragma unroll
-    for (int k = 0; k < TP; ++k) {
-      nvalid[k] = vlen - tok0[k];
-      interior[k] = okp[k] && (tok0[k] + kBlockSize - 1 <= minlim) &&
-                    (tok0[k] + p.wspan >= vlen) && (nvalid[k] >= kBlockSize);
-      mlo[k] = mhi[k] = 0xffffffffu;
-      if (nvalid[k] < kBlockSize) {
-        const int nv = nvalid[k];
-        // tokens behind the low / high halves of the first and second A register pairs
-        const int t0 = KV8 ? 4 * q4 : 2 * q4, t2 = KV8 ? 4 * q4 + 2 : 2 * q4 + 8;
-        mlo[k] = (t0 < nv ? 0x0000ffffu : 0u) | (t0 + 1 < nv ? 0xffff0000u : 0u);
-        mhi[k] = (t2 < nv ? 0x0000ffffu : 0u) | (t2 + 1 < nv ? 0xffff0000u : 0u);
-      }
-    }
-
-    uint32_t bh0[TP][NT], bh1[TP][NT], bl0[TP][NT], bl1[TP][NT];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      // lane holds S^T[j0][n], S^T[j0][n+1], S^T[j0+8][n], S^T[j0+8][n+1] of each
-      // page, n = rbase + 8j + 2q4 (t[k][0..3] in that order)
-      float t[TP][4];
-      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
-#pragma unroll
-      for (int k = 0; k < TP; ++k) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) t[k][e] = (sa[k][j][e] + sb[k][j][e]) * sl2;
-        if (!okp[k]) {
-          t[k][0] = t[k][1] = t[k][2] = t[k][3] = -CUDART_INF_F;
-        } else if (!interior[k]) {
-          const int j0 = tok0[k] + srow0, j1 = tok0[k] + srow1;
-          const unsigned u0 = static_cast<unsigned>(j0), u1 = static_cast<unsigned>(j1);
-          t[k][0] = (static_cast<unsigned>(lim0[j]) - u0 < p.wcap) ? t[k][0] : -CUDART_INF_F;
-          t[k][1] = (static_cast<unsigned>(lim1[j]) - u0 < p.wcap) ? t[k][1] : -CUDART_INF_F;
-          t[k][2] = (static_cast<unsigned>(lim0[j]) - u1 < p.wcap) ? t[k][2] : -CUDART_INF_F;
-          t[k][3] = (static_cast<unsigned>(lim1[j]) - u1 < p.wcap) ? t[k][3] : -CUDART_INF_F;
-        }
-        mx0 = fmaxf(mx0, fmaxf(t[k][0], t[k][2]));
-        mx1 = fmaxf(mx1, fmaxf(t[k][1], t[k][3]));
-      }
-
-      // online softmax (log2 domain), statistics per row.  The reference max m
-      // only moves when a score exceeds it by more than 8 (so every weight
-      // 2^(t - m) stays <= 256); the accumulators are rescaled only then.
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      const bool up0 = mx0 > m0[j] + 8.f, up1 = mx1 > m1[j] + 8.f;
-      if (__any_sync(0xffffffffu, up0 || up1)) {
-        const float al0 = up0 ? hw_exp2(m0[j] - mx0) : 1.f;
-        const float al1 = up1 ? hw_exp2(m1[j] - mx1) : 1.f;
-        if (up0) m0[j] = mx0;
-        if (up1) m1[j] = mx1;
-        l0[j] *= al0;
-        l1[j] *= al1;
-#pragma unroll
-        for (int mt = 0; mt < Gm::kKSteps; ++mt) {
-          acc[j][mt][0] *= al0;
-          acc[j][mt][1] *= al1;
-          acc[j][mt][2] *= al0;
-          acc[j][mt][3] *= al1;
-        }
-      }
-      const float mu0 = (m0[j] == -CUDART_INF_F) ? 0.f : m0[j];
-      const float mu1 = (m1[j] == -CUDART_INF_F) ? 0.f : m1[j];
-#pragma unroll
-      for (int k = 0; k < TP; ++k) {
-        const float p0 = hw_exp2(t[k][0] - mu0), p1 = hw_exp2(t[k][1] - mu1);
-        const float p2 = hw_exp2(t[k][2] - mu0), p3 = hw_exp2(t[k][3] - mu1);
-        l0[j] += p0 + p2;
-        l1[j] += p1 + p3;
-        if constexpr (KV8) {
-          // P^T as one f16 B operand (transposed 8x8 blocks)
-          bh0[k][j] = movmatrix_trans(half2_bits(__floats2half2_rn(p0, p1)));
-          bh1[k][j] = movmatrix_trans(half2_bits(__floats2half2_rn(p2, p3)));
-          continue;
-        }
-        // P^T as B operands: bf16 high part and bf16 residual, transposed 8x8 blocks
-        const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
-        const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
-        const float2 f01 = __bfloat1622float2(h01);
-        const float2 f23 = __bfloat1622float2(h23);
-        const __nv_bfloat162 r01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
-        const __nv_bfloat162 r23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
-        bh0[k][j] = movmatrix_trans(bf162_bits(h01));
-        bh1[k][j] = movmatrix_trans(bf162_bits(h23));
-        bl0[k][j] = movmatrix_trans(bf162_bits(r01));
-        bl1[k][j] = movmatrix_trans(bf162_bits(r23));
-      }
-    }
-
-    // O^T[D x 8] += V_page^T . P^T per page and n-tile
-#pragma unroll
-    for (int k = 0; k < TP; ++k) {
-      if (!okp[k]) continue;
-      auto pv = [&](auto tail) {
-        if constexpr (KV8) {
-          // transposed V: rows are head dims; ldmatrix c covers dims 32c .. 32c+31
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(r0, r1, r2, r3, vb[k] + voff[c]);
-            uint32_t a[2][4];
-            a[0][0] = e4m3x2_to_f16x2(r0);
-            a[0][2] = e4m3x2_to_f16x2(r0 >> 16);
-            a[0][1] = e4m3x2_to_f16x2(r1);
-            a[0][3] = e4m3x2_to_f16x2(r1 >> 16);
-            a[1][0] = e4m3x2_to_f16x2(r2);
-            a[1][2] = e4m3x2_to_f16x2(r2 >> 16);
-            a[1][1] = e4m3x2_to_f16x2(r3);
-            a[1][3] = e4m3x2_to_f16x2(r3 >> 16);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if constexpr (decltype(tail)::value) {
-                a[h][0] &= mlo[k];
-                a[h][1] &= mlo[k];
-                a[h][2] &= mhi[k];
-                a[h][3] &= mhi[k];
-              }
-#pragma unroll
-              for (int j = 0; j < NT; ++j)
-                mma_f16_16816(acc[j][2 * c + h], a[h][0], a[h][1], a[h][2], a[h][3],
-                              bh0[k][j], bh1[k][j]);
-            }
-          }
-          return;
-        }
-#pragma unroll
-        for (int mt = 0; mt < Gm::kKSteps; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(a0, a1, a2, a3, vb[k] + (mt >> 2) * Gm::kHalfBytes + voff[mt & 3]);
-          if constexpr (decltype(tail)::value) {
-            a0 &= mlo[k];
-            a1 &= mlo[k];
-            a2 &= mhi[k];
-            a3 &= mhi[k];
-          }
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bh0[k][j], bh1[k][j]);
-            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, bl0[k][j], bl1[k][j]);
-          }
-        }
-      };
-      if (nvalid[k] < kBlockSize)
-        pv(std::true_type{});
-      else
-        pv(std::false_type{});
-    }
+    attend_step<D, NT, TP, KV8, kQRegs>(st, okp, kb, vb, tok0, qf, qrow, koff, voff, lim0, lim1,
+                                        minlim, vlen, sl2, srow0, srow1, q4, p);
     __syncwarp();
     if (lane == 0) {
 #pragma unroll

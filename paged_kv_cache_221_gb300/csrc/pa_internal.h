@@ -14,6 +14,8 @@ enum : unsigned { kErrBounds = 1u, kErrTimeout = 2u };
 constexpr int kBlockSize = 16;        // tokens per physical block (the only size built)
 constexpr int kStages = 8;            // pages in flight per CTA (multiple of every PL)
 constexpr int kMaxRows = 64;          // query rows per CTA (8 n-tiles of 8)
+constexpr int kStreamMaxSeqs = 256;   // persistent decode kernel: sequences its unit list holds
+constexpr int kStreamMaxPpb = 256;    // persistent decode kernel: pages per partition
 constexpr int kMaxPartitions = 4096;  // split-KV partitions per sequence (merge smem bound)
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr int kMaxSpecVocab = 1 << 19;  // speculative acceptance: largest vocabulary
@@ -51,7 +53,22 @@ struct AttnParams {
   unsigned long long timeout_ns;  // limit of every pipeline wait
   int* unit_counter;              // tcgen05 kernel: next work unit to claim (zeroed before the
                                   //   launch), or nullptr for a fixed round-robin order
+  void* stream_ctl;               // persistent decode kernel: its StreamCtl in the scratch,
+                                  //   or nullptr (no scratch: fixed order)
 };
+
+// Claim state of the persistent decode kernel, kept in the split-KV scratch:
+// a tag and the next unit-list position to hand out.  When the tag is present
+// at launch, `next` is zero and CTAs claim positions from it; the split-KV merge
+// that follows every such launch sets `next` back to zero and writes the tag.
+// Without the tag (scratch not yet used by this kernel, or overwritten since)
+// the launch takes positions in a fixed order and leaves `next` untouched.
+struct StreamCtl {
+  unsigned long long tag;
+  int next;
+  int pad;
+};
+constexpr unsigned long long kStreamTag = 0x70615F7374726D31ull;
 
 // Split-KV scratch bytes a call with these sizes needs (partition_size 0 = the
 // library default for this kv-head count).
@@ -80,6 +97,17 @@ cudaError_t launch_attn_group8_d64(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
 cudaError_t launch_attn_group8_d128(const CUtensorMap& tk, const CUtensorMap& tv,
                                     const AttnParams& p, int rows, dim3 grid, cudaStream_t s);
+// Persistent decode kernel (pa_attn_stream.cuh): per-sequence mode, at most 8
+// query rows per kv head, at most kStreamMaxSeqs sequences and kStreamMaxPpb
+// pages per partition; `max_units` bounds the work units.  Unless `always`, it
+// runs only where it measured faster than the one-CTA-per-unit kernel (FP8
+// pages, or at least 4 units per resident CTA); *launched says whether it ran.
+cudaError_t launch_stream_d64(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                              int rows, long long max_units, bool kv8, bool always,
+                              cudaStream_t s, bool* launched);
+cudaError_t launch_stream_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                               int rows, long long max_units, bool kv8, bool always,
+                               cudaStream_t s, bool* launched);
 // tcgen05 kernel (head_dim 128, bf16 pages, 17-32 query rows per kv head).
 cudaError_t launch_attn_tc_d128(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                                 int rows, dim3 grid, cudaStream_t s, bool overlap_previous);
@@ -119,6 +147,8 @@ cudaError_t take_error_group8_d64(unsigned* bits);
 cudaError_t take_error_group8_d128(unsigned* bits);
 cudaError_t take_error_spec(unsigned* bits);
 cudaError_t take_error_attn_tc_d128(unsigned* bits);
+cudaError_t take_error_stream_d64(unsigned* bits);
+cudaError_t take_error_stream_d128(unsigned* bits);
 cudaError_t take_error_misc(unsigned* bits);
 
 }  // namespace pa

@@ -177,6 +177,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   __shared__ float s_ms[kMergeWarps][2];
   const int W = warps_per_row;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (p.stream_ctl != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+    // The persistent decode kernel has made its last claim: reset its counter
+    // for the next launch on this scratch.
+    grid_dependency_wait();
+    StreamCtl* ctl = static_cast<StreamCtl*>(p.stream_ctl);
+    ctl->next = 0;
+    __threadfence();
+    ctl->tag = kStreamTag;
+  }
   const int rows_per_cta = kMergeWarps / W;
   const int rows = p.G * p.T;
   const int chunks = (rows + rows_per_cta - 1) / rows_per_cta;

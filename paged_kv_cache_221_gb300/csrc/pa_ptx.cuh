@@ -97,6 +97,28 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy; the bytes past `src_bytes` (0 or 16) are
+// zero-filled, so src_bytes = 0 writes a zero chunk without reading `src`.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on the mbarrier once every cp.async this thread issued so far has
+// landed (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 // ---------------------------------------------------------------- exp2
 // 2^x by the hardware approximation (PTX ex2.approx, relative error below
 // 2^-22, subnormal results flushed); 2^-inf = +0.

@@ -1,0 +1,197 @@
+"""The persistent decode kernel (at most 8 query rows per kv head) against the
+one-CTA-per-unit kernel and the fp64 oracle.
+
+The persistent kernel runs a different schedule (a dense largest-first unit
+list, units claimed from a counter or taken in a fixed order, pages streamed across unit
+boundaries) but each unit's arithmetic is that of the one-CTA-per-unit kernel:
+page lane q takes the unit's pages q, q + PL, ... and the lanes merge in the same
+order.  So its output must be bit-identical to the one-CTA-per-unit kernel's
+(PA_DECODE_KERNEL=persistent and =per_unit select them; unset, the library
+chooses), and within the bf16 tolerance of the
+oracle (max abs error <= 1e-2 or one bf16 ulp of the oracle value, whichever is
+larger; relative L2 error <= 2e-3).
+
+Cases cover the schedule's edges: ragged lengths around partition boundaries,
+many partitions per sequence and single-partition sequences in one batch, one
+sequence, partition sizes whose split needs scratch (units claimed from the
+counter) and ones that need none (a fixed order), GQA ratios 1, 4 and 8 and two
+query tokens, head_dim 64 and 128, FP8 pages, the fused append, sliding
+windows, the 256-sequence limit of the in-CTA unit list and one sequence more
+(the one-CTA-per-unit kernel then runs), and the full 8B- and 70B-shape batches.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import fp8 as F
+from oracle import oracle as O
+from oracle import window as WIN
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():          # collected on CPU-only hosts, never run there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import __graft_entry__  # noqa: E402
+
+__graft_entry__.build()
+
+import paged_kv_cache_221_gb300 as pa  # noqa: E402
+from gpu_util import Dev, assert_close, bits, to_dev  # noqa: E402
+
+LENS = [1, 15, 16, 17, 100, 255, 256, 257, 700, 1023, 1024, 1025, 2047, 2048, 2049, 3000, 5000]
+
+
+@pytest.fixture(autouse=True)
+def no_device_error():
+    yield
+    assert pa.get_device_error() == 0, "device error word was set"
+
+
+def both(monkeypatch, run):
+    """run() with the persistent kernel and with the one-CTA-per-unit kernel; the two
+    outputs must be bit-identical.  Returns the persistent kernel's output."""
+    monkeypatch.setenv("PA_DECODE_KERNEL", "persistent")
+    a = run()
+    torch.cuda.synchronize()
+    monkeypatch.setenv("PA_DECODE_KERNEL", "per_unit")
+    b = run()
+    torch.cuda.synchronize()
+    monkeypatch.delenv("PA_DECODE_KERNEL")
+    np.testing.assert_array_equal(bits(a), bits(b))
+    return a
+
+
+@pytest.mark.parametrize("hq,hkv,T,D", [(32, 8, 1, 128), (64, 8, 1, 128), (8, 8, 1, 128),
+                                        (16, 8, 2, 128), (32, 8, 1, 64), (16, 2, 1, 64)])
+def test_lengths_and_partitions(monkeypatch, hq, hkv, T, D):
+    w = W.build("stream_lens", [max(L, T) for L in LENS], num_q_heads=hq, num_kv_heads=hkv,
+                head_dim=D, num_query_tokens=T, seed=hq + 3 * T + D)
+    ref, _, _ = O.run_workload(w)
+    d = Dev(w)
+    d.reshape()
+    for ps in (16, 48, 128, 1536, 0, 8192):
+        out = both(monkeypatch, lambda: d.attend(partition_size=ps))
+        assert_close(out, ref, what=f"{hq}/{hkv} T{T} D{D} ps{ps}")
+
+
+def test_one_sequence(monkeypatch):
+    w = W.build("stream_one", [4097], num_q_heads=32, num_kv_heads=8, head_dim=128, seed=5)
+    ref, _, _ = O.run_workload(w)
+    d = Dev(w)
+    d.reshape()
+    for ps in (16, 256, 0):
+        assert_close(both(monkeypatch, lambda: d.attend(partition_size=ps)), ref,
+                     what=f"one sequence ps{ps}")
+
+
+@pytest.mark.parametrize("ps", [0, 64, 272])
+def test_fused_append(monkeypatch, ps):
+    w = W.build("stream_append", LENS, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=9)
+    ref, kref, vref = O.run_workload(w)
+    outs = []
+    for mode in ("persistent", "per_unit"):
+        monkeypatch.setenv("PA_DECODE_KERNEL", mode)
+        d = Dev(w)                           # fresh pools: the append writes them
+        outs.append(bits(d.attend_append(partition_size=ps)))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits(d.k), kref)
+        np.testing.assert_array_equal(bits(d.v), vref)
+    monkeypatch.delenv("PA_DECODE_KERNEL")
+    np.testing.assert_array_equal(outs[0], outs[1])
+    out = torch.from_numpy(outs[0].view(np.int16)).view(torch.bfloat16)
+    assert_close(out, ref, what=f"append ps{ps}")
+
+
+@pytest.mark.parametrize("ps", [0, 96])
+def test_fp8_pages(monkeypatch, ps):
+    w = W.fp8_variant(W.build("stream_fp8", LENS, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                              seed=21), seed=2)
+    k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
+                               w.k_scale, w.v_scale, 16)
+    ref = F.paged_attention(w.q, k, v, w.k_scale, w.v_scale, w.block_tables, w.context_lens,
+                            w.scale, w.num_kv_heads, 16)
+    q, kc, vc = to_dev(w.q), to_dev(k), to_dev(v)
+    ks, vs = to_dev(w.k_scale), to_dev(w.v_scale)
+    tables, lens = to_dev(w.block_tables), to_dev(w.context_lens)
+    out = both(monkeypatch, lambda: pa.verify_fp8(q, kc, vc, ks, vs, tables, lens,
+                                                  w.max_context_len, w.scale, ps))
+    assert_close(out, ref, what=f"fp8 ps{ps}")
+
+
+@pytest.mark.parametrize("window", [1, 16, 17, 600])
+def test_windows(monkeypatch, window):
+    w = W.build("stream_win", LENS, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=31)
+    ref, _, _ = WIN.run_workload(w, window)
+    d = Dev(w)
+    for ps in (0, 64):
+        def run():
+            return pa.attention(d.q, d.k, d.v, d.tables, d.lens, w.max_context_len, w.scale, ps,
+                                None, None, d.new_key, d.new_value, window_size=window)
+        # the fused append rewrites the same values on every call
+        assert_close(both(monkeypatch, run), ref, what=f"window {window} ps{ps}")
+
+
+@pytest.mark.parametrize("B", [256, 257])
+def test_unit_list_limit(monkeypatch, B):
+    rng = np.random.default_rng(B)
+    lens = rng.integers(1, 3000, size=B)
+    w = W.build("stream_many", lens, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=B)
+    ref, _, _ = O.run_workload(w)
+    d = Dev(w)
+    d.reshape()
+    for ps in (256, 0):
+        assert_close(both(monkeypatch, lambda: d.attend(partition_size=ps)), ref,
+                     what=f"{B} sequences ps{ps}")
+
+
+@pytest.mark.parametrize("name", ["decode_8b", "decode_70b"])
+def test_full_size_bit_identical(monkeypatch, name):
+    """The benchmark's batches in its launch configuration (fused append, default
+    partitions), bf16 and FP8 pages; the oracle comparison of every row of these
+    is in the full-size parity tests."""
+    w = W.FULL[name]()
+    outs = []
+    for mode in ("persistent", "per_unit"):
+        monkeypatch.setenv("PA_DECODE_KERNEL", mode)
+        outs.append(bits(Dev(w).attend_append()))
+    np.testing.assert_array_equal(outs[0], outs[1])
+    w8 = W.fp8_variant(w, seed=0)
+    outs = []
+    for mode in ("persistent", "per_unit"):
+        monkeypatch.setenv("PA_DECODE_KERNEL", mode)
+        q, kc, vc = to_dev(w8.q), to_dev(w8.k_codes), to_dev(w8.v_codes)
+        out = pa.verify_fp8(q, kc, vc, to_dev(w8.k_scale), to_dev(w8.v_scale),
+                            to_dev(w8.block_tables), to_dev(w8.context_lens),
+                            w8.max_context_len, w8.scale, w8.partition_size, None, None,
+                            to_dev(w8.new_key), to_dev(w8.new_value))
+        outs.append(bits(out))
+    monkeypatch.delenv("PA_DECODE_KERNEL")
+    np.testing.assert_array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xFF])
+def test_claim_modes_on_one_scratch(monkeypatch, fill):
+    """The first launch on a scratch takes units in a fixed order and leaves the claim
+    counter ready (the split-KV merge resets it); the launches after it claim units from
+    the counter.  Every launch gives the same bits as the one-CTA-per-unit kernel."""
+    rng = np.random.default_rng(fill + 3)
+    w = W.build("stream_claim", rng.integers(1, 4000, size=96), num_q_heads=32,
+                num_kv_heads=8, head_dim=128, seed=fill + 3)
+    ref, _, _ = O.run_workload(w)
+    d = Dev(w)
+    d.reshape()
+    ps = 512
+    need = pa.workspace_size(w.num_seqs, w.num_q_heads, 1, w.max_context_len, w.head_dim, 16,
+                             ps, 0)
+    monkeypatch.setenv("PA_DECODE_KERNEL", "per_unit")
+    want = bits(d.attend(partition_size=ps))
+    monkeypatch.setenv("PA_DECODE_KERNEL", "persistent")
+    ws = torch.full((max(need, 256),), fill, dtype=torch.uint8, device="cuda")
+    for i in range(4):
+        out = d.attend(partition_size=ps, workspace=ws)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits(out), want, err_msg=f"launch {i}")
+    monkeypatch.delenv("PA_DECODE_KERNEL")
+    assert_close(out, ref, what="claim modes")
