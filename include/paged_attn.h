@@ -31,8 +31,8 @@
  *     bf16 (round to nearest even) once.
  *
  * Ownership: the caller owns every buffer.  The library never allocates or
- * frees device memory and keeps no per-call state; `workspace` is scratch the
- * caller provides (its size comes from pa_workspace_size).
+ * frees device memory and keeps no per-call state on the host; `workspace` is
+ * scratch the caller provides (its size comes from pa_workspace_size).
  *
  * Execution: every call only validates its arguments on the host, then
  * enqueues kernels on `stream` and returns; it never synchronises (except
@@ -125,7 +125,13 @@ int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_le
  * log-sum-exp rule by a second kernel; this needs `workspace` of at least
  * pa_workspace_size(...) bytes.  The workspace needs no initialisation (every
  * partial is written before it is read) and may be reused by later calls on
- * the same stream.  With partition_size = 0 and workspace == NULL every
+ * the same stream.  Its last 256 bytes also carry, from one call to the next,
+ * the work-claim counter of the persistent decode kernel (at most 8 query rows
+ * per kv head): a tagged counter that the merge kernel zeroes at the end of
+ * each call; a workspace that is new or was overwritten in between lacks the
+ * tag, and the next call then takes work units in a fixed order and sets the
+ * tag.  Two calls in flight at once must not share a workspace (their
+ * partials would collide anyway).  With partition_size = 0 and workspace == NULL every
  * sequence is processed whole (no scratch, fewer parallel units).  With an
  * explicit partition_size that needs scratch, a missing or short workspace
  * returns PA_ERR_WORKSPACE.
