@@ -36,7 +36,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "paged decode-attention KV-read GB/s vs GB300 HBM peak; seq-steps/sec"
 L2_BYTES = 129 * 1000 * 1000     # GB300 L2
-KERNEL_SOURCES = ["pa_attn.cuh", "pa_ptx.cuh"]   # the attention kernel template and its PTX
+KERNEL_SOURCES = ["pa_attn.cuh", "pa_attn_stream.cuh", "pa_ptx.cuh"]   # attention kernels, PTX
 KERNEL_PARAMS = "pa_internal.h"                  # its constants and AttnParams (up to the struct end)
 WORKLOAD_DESC = {
     "tiny": "2 seqs (ctx 37, 100), 4 q = 4 kv heads, head_dim 64, 16-block pool",
@@ -129,9 +129,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per launch of the attention kernel from a committed ncu summary, if the
-    kernel sources have not changed since it was captured."""
+def recorded_capture(workload):
+    """The committed ncu record of the attention call on this workload (its kernels and
+    their DRAM bytes per launch), if the kernel sources have not changed since it was
+    captured; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -140,7 +141,7 @@ def recorded_traffic(workload):
     e = d.get(workload)
     if not e or e.get("kernel_src_sha") != kernel_source_hash():
         return None
-    return e.get("dram_bytes_per_launch")
+    return e
 
 
 class ClockSampler:
@@ -575,11 +576,13 @@ class Case:
 
     def roofline(self, attn_avg, peak, peak_kind):
         achieved = self.kv_bytes / (attn_avg * 1e-3) / 1e9
+        # the recorded captures are of full-context launches
+        rec = recorded_capture(self.w.name) if self.window <= 0 else None
+        kern = rec["kernel"] if rec else "attention kernel"
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
-                # the recorded captures are of full-context launches
-                "traffic": recorded_traffic(self.w.name) if self.window <= 0 else None,
-                "kernel": "attention call (paged_attn_kernel + splitkv_reduce_kernel)",
+                "traffic": rec["dram_bytes_per_launch"] if rec else None,
+                "kernel": f"attention call ({kern} + splitkv_reduce_kernel)",
                 "peak_source": f"{peak_kind} hbm_gbs",
                 "launch_ms_avg": round(attn_avg, 5)}
 
