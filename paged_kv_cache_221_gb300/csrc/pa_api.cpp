@@ -305,8 +305,8 @@ pa_status run_attention(const AttnArgs& a) {
     dim3 grid(static_cast<unsigned>(units), 1, 1);
     const StreamMode mode = stream_kernel_mode();
     bool launched = false;
-    if (!grouped && rows <= 8 && a.num_seqs <= kStreamMaxSeqs && plan.ppb <= kStreamMaxPpb &&
-        mode != kStreamNever) {
+    if (!grouped && (rows <= 8 || (rows >= 17 && rows <= 24)) && a.num_seqs <= kStreamMaxSeqs &&
+        plan.ppb <= kStreamMaxPpb && mode != kStreamNever) {
       // Claim state 16 bytes into the counter area (the tcgen05 kernel's
       // counter is the first 4 bytes).
       if (plan.ws_bytes > 0)

@@ -42,10 +42,10 @@ struct StreamUnit {
 };
 
 
-template <int D, int NT, bool KV8>
+template <int D, int NT, int NTW, int PL, bool KV8>
 struct StreamSmem {
   using Gm = Geo<D, KV8>;
-  static constexpr int kRows = 8 * NT;
+  static constexpr int kRows = 8 * NT * NTW;
   static constexpr int kQBytes = kRows * Gm::kQStride * 2;        // one query-row buffer
   static constexpr int kQOff = Gm::kNS * Gm::kStageBytes;         // two buffers
   static constexpr int kRecOff = kQOff + 2 * kQBytes;             // two unit records
@@ -58,11 +58,15 @@ struct StreamSmem {
   static constexpr int kNumBars = 2 * Gm::kNS + 5;
   static constexpr int kOkOff = kBarOff + kNumBars * 8;
   static constexpr int kFlagOff = kOkOff + Gm::kNS * 4;
-  static constexpr int kBytes = kFlagOff + 16;
-  static constexpr int kAlloc = kBytes + 1024;                    // room to align the base to 1 KB
-  // merge partial of one page lane: m[8NT], l[8NT], O[8NT][kOStride] (in its kept stage)
+  // merge partial of one (page lane, row column): m[8NT], l[8NT], O[8NT][kOStride].
+  // One column: in the page lane's kept ring stage.  Several: in a buffer of their own.
   static constexpr int kMergeFloats = 16 * NT + 8 * NT * Gm::kOStride;
-  static_assert(kMergeFloats * 4 <= Gm::kStageBytes, "a page lane's partial fits in one stage");
+  static constexpr bool kKeepStage = NTW == 1;
+  static constexpr int kMergeOff = (kFlagOff + 16 + 15) / 16 * 16;
+  static constexpr int kBytes = kMergeOff + (kKeepStage ? 0 : PL * NTW * kMergeFloats * 4);
+  static constexpr int kAlloc = kBytes + 1024;                    // room to align the base to 1 KB
+  static_assert(!kKeepStage || kMergeFloats * 4 <= Gm::kStageBytes,
+                "a page lane's partial fits in one stage");
   static_assert(kQOff % 16 == 0 && Gm::kQStride * 2 % 16 == 0, "16-byte query chunks");
 };
 
@@ -177,15 +181,18 @@ template <int D, class C, bool KV8>
 __global__ void __launch_bounds__(C::kThreads, C::MINB)
     paged_attn_stream_kernel(const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
-  static_assert(C::NTW == 1, "one column of query rows");
-  constexpr int NT = C::NT, PL = C::PL;
-  constexpr int NCW = PL;                    // consumer warps (page lanes)
+  constexpr int NT = C::NT, NTW = C::NTW, PL = C::PL;
+  constexpr int NCW = NTW * PL;              // consumer warps: NTW row columns x PL page lanes
   constexpr int NCT = NCW * 32;
   using Gm = Geo<D, KV8>;
-  using Sm = StreamSmem<D, NT, KV8>;
+  using Sm = StreamSmem<D, NT, NTW, PL, KV8>;
   constexpr int NS = Gm::kNS;
   constexpr int PPS = Gm::kPPS;              // pages per ring stage
-  constexpr int TP = PPS;                    // pages per consumer step (one stage)
+  // ring stages per consumer step (as in the one-CTA-per-unit kernel; FP8 pages:
+  // one stage of two pages), and pages per step
+  constexpr int TPI = KV8 ? 1 : C::TP;
+  constexpr int TP = TPI * PPS;
+  static_assert(!Sm::kKeepStage || TPI == 1, "a kept stage ends a one-stage step");
   constexpr int CH = D / 8;                  // 16-byte chunks per query row
   static_assert(NS % PL == 0, "each stage is always consumed by the same page lane");
 
@@ -220,7 +227,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], NTW);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ufull[i], 33);              // 32 cp.async arrivals + the record writer
@@ -561,7 +568,9 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
                     ord, cnt, meta);
     if (lane == 0) mbar_arrive(lready);
   }
-  const int pl = warp;                       // page lane: items pl, pl + PL, ... (mod PL)
+  const int col = warp % NTW;                // rows 8*NT*col .. 8*NT*(col+1)-1
+  const int pl = warp / NTW;                 // page lane: items pl, pl + PL, ... (mod PL)
+  const int rbase = 8 * NT * col;
   const int gid = lane >> 2, q4 = lane & 3;
   float sl2 = p.scale_log2;
   float out_scale = 1.f;
@@ -622,8 +631,9 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
       sl2 = p.scale_log2 * p.k_scale[g];
       out_scale = p.v_scale[g];
     }
-    const uint32_t qrow = smem_u32(qb) + static_cast<uint32_t>((lane & 7) * Gm::kQStride * 2 +
-                                                               (lane >> 3) * 16);
+    const uint32_t qrow = smem_u32(qb) + static_cast<uint32_t>(
+                                             (rbase + (lane & 7)) * Gm::kQStride * 2 +
+                                             (lane >> 3) * 16);
     uint32_t qf[NT][Gm::kKSteps][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -634,11 +644,12 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     __syncwarp();
     if (lane == 0) mbar_arrive(&uempty[buf]);
 
-    // visibility limits of this lane's rows 8j + 2q4 (+1); padding rows see everything
+    // visibility limits of this lane's rows rbase + 8j + 2q4 (+1); padding rows
+    // see everything
     int lim0[NT], lim1[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const int n0 = 8 * j + 2 * q4, n1 = n0 + 1;
+      const int n0 = rbase + 8 * j + 2 * q4, n1 = n0 + 1;
       lim0[j] = n0 < nrows ? r.vlen - T + (n0 / G) % T : 0x7fffffff;
       lim1[j] = n1 < nrows ? r.vlen - T + (n1 / G) % T : 0x7fffffff;
     }
@@ -677,30 +688,55 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     auto lane_first = [&](int q) { return item0 + q; };
     auto lane_last = [&](int q) { return item0 + q + ((nitems - 1 - q) / PL) * PL; };
     const int my_first = lane_first(pl);
-    for (int gi = my_first; gi < iend; gi += PL) {
-      const int s = gi % NS;
-      const uint32_t ph = static_cast<uint32_t>(gi / NS) & 1u;
-      if (!aborted && !mbar_wait(&full[s], ph, p.timeout_ns)) aborted = true;
-      const bool ok = !aborted && stage_ok[s];
-      const uint32_t sb = smem_u32(stages + s * Gm::kStageBytes);
+    // Steps of TPI items of this lane (gi, gi + PL): one softmax update per step.
+    for (int gi = my_first; gi < iend; gi += TPI * PL) {
+      const int nstep = (TPI == 2 && gi + PL < iend) ? 2 : 1;
       bool okp[TP];
       uint32_t kb[TP], vb[TP];
-      int tok0[TP];
+      int tok0[TP], sidx[TPI];
 #pragma unroll
-      for (int u = 0; u < PPS; ++u) {
-        const int pg = (gi - item0) * PPS + u;
-        okp[u] = ok && pg < r.npages;
-        kb[u] = sb + u * Gm::kPageBytes;
-        vb[u] = sb + (PPS + u) * Gm::kPageBytes;
-        tok0[u] = (r.pg0 + pg) * kBlockSize;
+      for (int si = 0; si < TPI; ++si) {
+        sidx[si] = -1;
+#pragma unroll
+        for (int u = 0; u < PPS; ++u) {
+          okp[si * PPS + u] = false;
+          kb[si * PPS + u] = vb[si * PPS + u] = 0;
+          tok0[si * PPS + u] = 0;
+        }
+        if (si < nstep) {
+          const int item = gi + si * PL;
+          const int s = item % NS;
+          if (!aborted && !mbar_wait(&full[s], static_cast<uint32_t>(item / NS) & 1u,
+                                     p.timeout_ns))
+            aborted = true;
+          const bool ok = !aborted && stage_ok[s];
+          const uint32_t sb = smem_u32(stages + s * Gm::kStageBytes);
+          sidx[si] = s;
+#pragma unroll
+          for (int u = 0; u < PPS; ++u) {
+            const int pg = (item - item0) * PPS + u;
+            okp[si * PPS + u] = ok && pg < r.npages;
+            kb[si * PPS + u] = sb + u * Gm::kPageBytes;
+            vb[si * PPS + u] = sb + (PPS + u) * Gm::kPageBytes;
+            tok0[si * PPS + u] = (r.pg0 + pg) * kBlockSize;
+          }
+        }
       }
       attend_step<D, NT, TP, KV8, kQRegs>(st, okp, kb, vb, tok0, qf, qrow, koff, voff, lim0,
                                           lim1, minlim, r.vlen, sl2, srow0, srow1, q4, p);
       __syncwarp();
-      if (gi + PL < iend && lane == 0) mbar_arrive(&empty[s]);   // the last stage is kept
+      if (lane == 0) {
+#pragma unroll
+        for (int si = 0; si < TPI; ++si) {
+          // with one row column the lane's last stage is kept for the merge
+          if (si < nstep && !(Sm::kKeepStage && gi + si * PL + PL >= iend))
+            mbar_arrive(&empty[sidx[si]]);
+        }
+      }
     }
 
-    // ---- unit end: merge the page lanes through their kept stages
+    // ---- unit end: merge the page lanes (through their kept stages with one row
+    // column, else through the merge buffer)
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
 #pragma unroll
@@ -709,9 +745,12 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
         st.l1[j] += __shfl_xor_sync(0xffffffffu, st.l1[j], o);
       }
     }
-    const int held = my_first < iend ? lane_last(pl) % NS : -1;
-    if (held >= 0) {
-      float* mbuf = reinterpret_cast<float*>(stages + held * Gm::kStageBytes);
+    const int held = (Sm::kKeepStage && my_first < iend) ? lane_last(pl) % NS : -1;
+    if (my_first < iend) {
+      float* mbuf = Sm::kKeepStage
+                        ? reinterpret_cast<float*>(stages + held * Gm::kStageBytes)
+                        : reinterpret_cast<float*>(smem + Sm::kMergeOff) +
+                              (pl * NTW + col) * Sm::kMergeFloats;
       float* ob = mbuf + 16 * NT;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
@@ -734,33 +773,41 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     if (aborted) s_stop[(k + 1) & 1] = 1;
     named_bar_sync(1, NCT);
     {
-      const float* mbq[PL];                  // partials of the page lanes that had pages
+      // partials of the page lanes that had pages (row column 0; the merge
+      // buffer holds the columns of one page lane side by side)
+      const float* mbq[PL];
 #pragma unroll
       for (int q = 0; q < PL; ++q) {
         mbq[q] = nullptr;
-        if (lane_first(q) < iend) {
-          mbq[q] = reinterpret_cast<const float*>(stages + (lane_last(q) % NS) * Gm::kStageBytes);
-        }
+        if (lane_first(q) < iend)
+          mbq[q] = Sm::kKeepStage
+                       ? reinterpret_cast<const float*>(stages +
+                                                        (lane_last(q) % NS) * Gm::kStageBytes)
+                       : reinterpret_cast<const float*>(smem + Sm::kMergeOff) +
+                             q * NTW * Sm::kMergeFloats;
       }
       for (int idx = threadIdx.x; idx < nrows * (D / 2); idx += NCT) {
-        const int n = idx / (D / 2);
+        const int n0 = idx / (D / 2);
         const int d = (idx % (D / 2)) * 2;
+        const int c = n0 / (8 * NT), n = n0 % (8 * NT);   // row column, row within it
+        const int cofs = c * Sm::kMergeFloats;
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int q = 0; q < PL; ++q)
-          if (mbq[q] != nullptr) M = fmaxf(M, mbq[q][n]);
+          if (mbq[q] != nullptr) M = fmaxf(M, mbq[q][cofs + n]);
         float Ls = 0.f, o0 = 0.f, o1 = 0.f;
         if (M != -CUDART_INF_F) {
 #pragma unroll
           for (int q = 0; q < PL; ++q) {
             if (mbq[q] == nullptr) continue;
-            const float f = exp2f(mbq[q][n] - M);
-            Ls += f * mbq[q][8 * NT + n];
-            o0 += f * mbq[q][16 * NT + n * Gm::kOStride + d];
-            o1 += f * mbq[q][16 * NT + n * Gm::kOStride + d + 1];
+            const float* mb = mbq[q] + cofs;
+            const float f = exp2f(mb[n] - M);
+            Ls += f * mb[8 * NT + n];
+            o0 += f * mb[16 * NT + n * Gm::kOStride + d];
+            o1 += f * mb[16 * NT + n * Gm::kOStride + d + 1];
           }
         }
-        const int t = (n / G) % T, hl = n % G;
+        const int t = (n0 / G) % T, hl = n0 % G;
         const size_t orow = (static_cast<size_t>(r.b) * T + t) * p.Hq + g * G + hl;
         if (r.direct) {
           const float inv = out_scale / Ls;
@@ -777,7 +824,9 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
     }
     // The kept stages were written and read through the generic proxy; the
     // producer's next TMA writes to them come after this fence and the release.
-    fence_proxy_async_smem();
+    // (With a merge buffer, the barrier keeps the next unit's partials from
+    // overwriting this one's before every thread has read them.)
+    if constexpr (Sm::kKeepStage) fence_proxy_async_smem();
     named_bar_sync(1, NCT);
     if (held >= 0 && lane == 0) mbar_arrive(&empty[held]);
     item0 = iend;
@@ -788,7 +837,7 @@ __global__ void __launch_bounds__(C::kThreads, C::MINB)
 // Resident CTAs per SM and SMs of the current device, queried once per device.
 template <int D, class C, bool KV8>
 cudaError_t stream_grid_limit(int* limit) {
-  constexpr int smem = StreamSmem<D, C::NT, KV8>::kAlloc;
+  constexpr int smem = StreamSmem<D, C::NT, C::NTW, C::PL, KV8>::kAlloc;
   auto kern = paged_attn_stream_kernel<D, C, KV8>;
   static std::atomic<int> cached[64];
   int dev = 0;
@@ -814,28 +863,40 @@ cudaError_t stream_grid_limit(int* limit) {
   return cudaSuccess;
 }
 
-// `max_units` bounds the work units (partitions x kv heads x sequences); the
-// grid is the smaller of it and the CTAs that fit on the device at once.
-// Unless `always`, the kernel is launched only with at least 4 units (bound)
-// per resident CTA: with fewer, long units (bf16 pages at 8B shape: 2 per CTA)
-// measured no faster than one CTA per unit.  *launched says whether it ran.
-template <int D, bool KV8>
-cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                          int rows, long long max_units, bool always, cudaStream_t s,
-                          bool* launched) {
-  using C = Cfg<1, 1, 4, 3>;
-  *launched = false;
-  if (rows <= 0 || rows > 8) return cudaErrorInvalidValue;
+template <int D, class C, bool KV8>
+cudaError_t launch_stream_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                              long long max_units, bool always, cudaStream_t s, bool* launched) {
   int limit = 0;
   cudaError_t e = stream_grid_limit<D, C, KV8>(&limit);
   if (e != cudaSuccess) return e;
   if (!always && max_units < 4ll * limit) return cudaSuccess;
   const int grid = static_cast<int>(std::min<long long>(std::max(1ll, max_units), limit));
-  constexpr int smem = StreamSmem<D, C::NT, KV8>::kAlloc;
+  constexpr int smem = StreamSmem<D, C::NT, C::NTW, C::PL, KV8>::kAlloc;
   paged_attn_stream_kernel<D, C, KV8><<<grid, C::kThreads, smem, s>>>(tk, tv, p);
   e = cudaGetLastError();
   *launched = e == cudaSuccess;
   return e;
+}
+
+// `rows` = query rows per kv head: at most 8 (decode; one row column, 3 CTAs
+// per SM) or 17-24 (verify; three row columns, 2 CTAs per SM, the layouts of the
+// one-CTA-per-unit kernel).  `max_units` bounds the work units (partitions x kv
+// heads x sequences); the grid is the smaller of it and the CTAs that fit on
+// the device at once.  Unless `always`, the kernel is launched only with at
+// least 4 units (bound) per resident CTA: with fewer, long units (bf16 pages at
+// 8B shape: 2 per CTA) measured no faster than one CTA per unit.  *launched
+// says whether it ran; other row counts never run here.
+template <int D, bool KV8>
+cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                          int rows, long long max_units, bool always, cudaStream_t s,
+                          bool* launched) {
+  *launched = false;
+  if (rows >= 1 && rows <= 8)
+    return launch_stream_cfg<D, Cfg<1, 1, 4, 3>, KV8>(tk, tv, p, max_units, always, s, launched);
+  if (rows >= 17 && rows <= 24)
+    return launch_stream_cfg<D, Cfg<1, 3, 2, 2, 2>, KV8>(tk, tv, p, max_units, always, s,
+                                                          launched);
+  return cudaSuccess;
 }
 
 }  // namespace pa

@@ -1,5 +1,5 @@
-"""The persistent decode kernel (at most 8 query rows per kv head) against the
-one-CTA-per-unit kernel and the fp64 oracle.
+"""The persistent attention kernel (at most 8 query rows per kv head, or 17-24 for
+speculative verify) against the one-CTA-per-unit kernel and the fp64 oracle.
 
 The persistent kernel runs a different schedule (a dense largest-first unit
 list, units claimed from a counter or taken in a fixed order, pages streamed across unit
@@ -15,9 +15,11 @@ Cases cover the schedule's edges: ragged lengths around partition boundaries,
 many partitions per sequence and single-partition sequences in one batch, one
 sequence, partition sizes whose split needs scratch (units claimed from the
 counter) and ones that need none (a fixed order), GQA ratios 1, 4 and 8 and two
-query tokens, head_dim 64 and 128, FP8 pages, the fused append, sliding
-windows, the 256-sequence limit of the in-CTA unit list and one sequence more
-(the one-CTA-per-unit kernel then runs), and the full 8B- and 70B-shape batches.
+query tokens, verify tiles of 18, 20 and 24 rows (three row columns and a merge
+buffer), head_dim 64 and 128, FP8 pages, the fused append, sliding windows,
+the 256-sequence limit of the in-CTA unit list and one sequence more (the
+one-CTA-per-unit kernel then runs), and the full 8B-, 70B-shape and verify
+batches.
 """
 import numpy as np
 import pytest
@@ -64,7 +66,9 @@ def both(monkeypatch, run):
 
 
 @pytest.mark.parametrize("hq,hkv,T,D", [(32, 8, 1, 128), (64, 8, 1, 128), (8, 8, 1, 128),
-                                        (16, 8, 2, 128), (32, 8, 1, 64), (16, 2, 1, 64)])
+                                        (16, 8, 2, 128), (32, 8, 1, 64), (16, 2, 1, 64),
+                                        (32, 8, 5, 128), (16, 8, 9, 128), (64, 8, 3, 128),
+                                        (24, 8, 6, 64)])
 def test_lengths_and_partitions(monkeypatch, hq, hkv, T, D):
     w = W.build("stream_lens", [max(L, T) for L in LENS], num_q_heads=hq, num_kv_heads=hkv,
                 head_dim=D, num_query_tokens=T, seed=hq + 3 * T + D)
@@ -86,9 +90,10 @@ def test_one_sequence(monkeypatch):
                      what=f"one sequence ps{ps}")
 
 
-@pytest.mark.parametrize("ps", [0, 64, 272])
-def test_fused_append(monkeypatch, ps):
-    w = W.build("stream_append", LENS, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=9)
+@pytest.mark.parametrize("ps,T", [(0, 1), (64, 1), (272, 1), (0, 5), (96, 5)])
+def test_fused_append(monkeypatch, ps, T):
+    w = W.build("stream_append", [max(L, T) for L in LENS], num_q_heads=32, num_kv_heads=8,
+                head_dim=128, num_query_tokens=T, seed=9 + T)
     ref, kref, vref = O.run_workload(w)
     outs = []
     for mode in ("persistent", "per_unit"):
@@ -104,10 +109,11 @@ def test_fused_append(monkeypatch, ps):
     assert_close(out, ref, what=f"append ps{ps}")
 
 
-@pytest.mark.parametrize("ps", [0, 96])
-def test_fp8_pages(monkeypatch, ps):
-    w = W.fp8_variant(W.build("stream_fp8", LENS, num_q_heads=32, num_kv_heads=8, head_dim=128,
-                              seed=21), seed=2)
+@pytest.mark.parametrize("ps,T", [(0, 1), (96, 1), (0, 5), (160, 5)])
+def test_fp8_pages(monkeypatch, ps, T):
+    w = W.fp8_variant(W.build("stream_fp8", [max(L, T) for L in LENS], num_q_heads=32,
+                              num_kv_heads=8, head_dim=128, num_query_tokens=T, seed=21 + T),
+                      seed=2)
     k, v = F.reshape_and_cache(w.new_key, w.new_value, w.k_codes, w.v_codes, w.slot_mapping,
                                w.k_scale, w.v_scale, 16)
     ref = F.paged_attention(w.q, k, v, w.k_scale, w.v_scale, w.block_tables, w.context_lens,
@@ -120,9 +126,10 @@ def test_fp8_pages(monkeypatch, ps):
     assert_close(out, ref, what=f"fp8 ps{ps}")
 
 
-@pytest.mark.parametrize("window", [1, 16, 17, 600])
-def test_windows(monkeypatch, window):
-    w = W.build("stream_win", LENS, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=31)
+@pytest.mark.parametrize("window,T", [(1, 1), (16, 1), (17, 1), (600, 1), (3, 5), (700, 5)])
+def test_windows(monkeypatch, window, T):
+    w = W.build("stream_win", [max(L, T) for L in LENS], num_q_heads=32, num_kv_heads=8,
+                head_dim=128, num_query_tokens=T, seed=31 + T)
     ref, _, _ = WIN.run_workload(w, window)
     d = Dev(w)
     for ps in (0, 64):
@@ -146,7 +153,7 @@ def test_unit_list_limit(monkeypatch, B):
                      what=f"{B} sequences ps{ps}")
 
 
-@pytest.mark.parametrize("name", ["decode_8b", "decode_70b"])
+@pytest.mark.parametrize("name", ["decode_8b", "decode_70b", "spec_verify"])
 def test_full_size_bit_identical(monkeypatch, name):
     """The benchmark's batches in its launch configuration (fused append, default
     partitions), bf16 and FP8 pages; the oracle comparison of every row of these
