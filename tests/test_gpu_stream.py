@@ -202,3 +202,28 @@ def test_claim_modes_on_one_scratch(monkeypatch, fill):
         np.testing.assert_array_equal(bits(out), want, err_msg=f"launch {i}")
     monkeypatch.delenv("PA_DECODE_KERNEL")
     assert_close(out, ref, what="claim modes")
+
+
+@pytest.mark.parametrize("bad", [0, 9])
+def test_context_above_bound_reports_bounds(monkeypatch, bad):
+    """A context above max_context_len: the persistent kernel sets the bounds bit, writes
+    nothing for that sequence and gives every other sequence its result.  Sequence 0's
+    first partitions open CTAs (their first record is then empty); sequence 9's come from
+    the unit list."""
+    monkeypatch.setenv("PA_DECODE_KERNEL", "persistent")
+    w = W.build("stream_bad", LENS, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=41)
+    ref, _, _ = O.run_workload(w)
+    d = Dev(w)
+    d.reshape()
+    lens = w.context_lens.copy()
+    lens[bad] = w.max_context_len + 16
+    d.lens = to_dev(lens)
+    keep = [b for b in range(w.num_seqs) if b != bad]
+    for ps in (64, 0):
+        out = torch.full_like(d.q, float("nan"))
+        pa.verify(d.q, d.k, d.v, d.tables, d.lens, w.max_context_len, w.scale, ps, None, out)
+        torch.cuda.synchronize()
+        assert pa.get_device_error() == 5
+        assert torch.isnan(out[bad].float()).all()
+        assert_close(out, ref, seqs=keep, what=f"bad length in sequence {bad}, ps{ps}")
+    monkeypatch.delenv("PA_DECODE_KERNEL")
