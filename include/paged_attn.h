@@ -38,6 +38,17 @@
  * enqueues kernels on `stream` and returns; it never synchronises (except
  * pa_get_device_error, which says so).
  *
+ * Kernels: per-sequence attention runs in a one-CTA-per-work-unit kernel or,
+ * for at most 8 or 17-24 query rows per kv head, in a persistent kernel whose
+ * CTAs stream units back to back (chosen for FP8 pages and for launches with
+ * at least 4 units per resident CTA).  Both give bit-identical results.  The
+ * environment variable PA_DECODE_KERNEL ("per_unit" or "persistent", read on
+ * every call) forces one of them; PA_VERIFY_KERNEL = "tcgen05" selects a
+ * tensor-memory kernel for 17-32 rows at head_dim 128 with bf16 pages (within
+ * the same tolerance of the exact result, not bit-identical, and slower on
+ * GB300 than the default).  Neither variable changes argument checks or
+ * scratch sizes.
+ *
  * Errors: argument errors are returned synchronously and nothing is launched.
  * A launch failure returns PA_ERR_CUDA.  Conditions only the device can see
  * (a block id outside the pool, a slot outside the pool, a context length
