@@ -87,6 +87,15 @@ const char* pa_status_string(int status);
 /* ABI version of this library (major*100 + minor). */
 int pa_version(void);
 
+/* Which kernel the last per-sequence attention launch made by this host thread
+ * used (a diagnostic; the choice is described under "Kernels" above):
+ * PA_KERNEL_NONE (no launch yet on this thread), PA_KERNEL_PER_UNIT (one CTA per
+ * work unit), PA_KERNEL_PERSISTENT, PA_KERNEL_TCGEN05.  Group (shared-prefix)
+ * launches do not change it.  No device work, no error. */
+enum { PA_KERNEL_NONE = 0, PA_KERNEL_PER_UNIT = 1, PA_KERNEL_PERSISTENT = 2,
+       PA_KERNEL_TCGEN05 = 3 };
+int pa_last_attention_kernel(void);
+
 /*
  * pa_reshape_and_cache — store the K and V vectors of `num_tokens` new tokens
  * into their cache slots: for token i with s = slot_mapping[i] >= 0,

@@ -416,6 +416,15 @@ def get_device_error(device=None) -> int:
     return int(library().pa_get_device_error(_stream(dev)))
 
 
+LAST_KERNEL_NAMES = {0: "none", 1: "per_unit", 2: "persistent", 3: "tcgen05"}
+
+
+def last_attention_kernel() -> str:
+    """The kernel of this thread's last per-sequence attention launch: "none",
+    "per_unit", "persistent" or "tcgen05" (a diagnostic)."""
+    return LAST_KERNEL_NAMES[int(library().pa_last_attention_kernel())]
+
+
 def selftest_wait_timeout(timeout_ns: int, device=None) -> None:
     """Launch the bounded-wait self test (read the outcome with get_device_error)."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \

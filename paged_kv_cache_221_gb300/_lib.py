@@ -44,6 +44,7 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [_i]),
     "pa_version": (_i, []),
+    "pa_last_attention_kernel": (_i, []),
     "pa_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "pa_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "pa_default_partition_size": (_i, [_i, _i, _i, _i]),

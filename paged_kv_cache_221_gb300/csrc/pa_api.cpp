@@ -74,6 +74,10 @@ bool encode_fp8_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k_base, const
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The kernel of this host thread's last per-sequence attention launch
+// (pa_last_attention_kernel).
+thread_local int g_last_kernel = PA_KERNEL_NONE;
+
 // Kernel for multi-query tiles of 17-32 query rows per kv head (speculative
 // verify) at head_dim 128 with bf16 pages: the mma.sync kernel, or the tcgen05
 // kernel when the environment variable PA_VERIFY_KERNEL is "tcgen05" (read on
@@ -304,9 +308,12 @@ pa_status run_attention(const AttnArgs& a) {
     if (units >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(units), 1, 1);
     const StreamMode mode = stream_kernel_mode();
+    // the tcgen05 kernel, when asked for, takes precedence for its tiles
+    const bool tc = !a.kv8 && a.head_dim == 128 && rows > 16 && rows <= 32 &&
+                    tensor_core_kernel_enabled();
     bool launched = false;
-    if (!grouped && (rows <= 8 || (rows >= 17 && rows <= 24)) && a.num_seqs <= kStreamMaxSeqs &&
-        plan.ppb <= kStreamMaxPpb && mode != kStreamNever) {
+    if (!grouped && !tc && (rows <= 8 || (rows >= 17 && rows <= 24)) &&
+        a.num_seqs <= kStreamMaxSeqs && plan.ppb <= kStreamMaxPpb && mode != kStreamNever) {
       // Claim state 16 bytes into the counter area (the tcgen05 kernel's
       // counter is the first 4 bytes).
       if (plan.ws_bytes > 0)
@@ -317,12 +324,13 @@ pa_status run_attention(const AttnArgs& a) {
               : launch_stream_d128(tk, tv, p, rows, units, a.kv8, always, a.stream, &launched);
       if (e != cudaSuccess) return PA_ERR_CUDA;
       if (!launched) p.stream_ctl = nullptr;
+      else g_last_kernel = PA_KERNEL_PERSISTENT;
     }
     if (!launched) {
       if (a.kv8) {
         e = a.head_dim == 64 ? launch_attn8_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                              : launch_attn8_d128(tk, tv, p, rows, grid, a.stream, group_launch);
-      } else if (a.head_dim == 128 && rows > 16 && rows <= 32 && tensor_core_kernel_enabled()) {
+      } else if (tc) {
         // With scratch, the persistent CTAs claim units from a counter zeroed here.
         if (plan.ws_bytes > 0) {
           p.unit_counter =
@@ -331,11 +339,13 @@ pa_status run_attention(const AttnArgs& a) {
           if (e != cudaSuccess) return PA_ERR_CUDA;
         }
         e = launch_attn_tc_d128(tk, tv, p, rows, grid, a.stream, group_launch);
+        g_last_kernel = PA_KERNEL_TCGEN05;
       } else {
         e = a.head_dim == 64 ? launch_attn_d64(tk, tv, p, rows, grid, a.stream, group_launch)
                              : launch_attn_d128(tk, tv, p, rows, grid, a.stream, group_launch);
       }
       if (e != cudaSuccess) return PA_ERR_CUDA;
+      if (!tc) g_last_kernel = PA_KERNEL_PER_UNIT;
     }
   }
   if (plan.ws_bytes > 0) {
@@ -384,7 +394,9 @@ const char* pa_status_string(int status) {
   }
 }
 
-int pa_version(void) { return 100; }
+int pa_version(void) { return 101; }
+
+int pa_last_attention_kernel(void) { return g_last_kernel; }
 
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache,
                                void* v_cache, const int64_t* slot_mapping, int num_tokens,

@@ -84,3 +84,4 @@ def assert_close(out, ref, seqs=None, what=""):
     assert over.max() <= 0 and rel <= MAX_REL_L2, \
         f"{what}: max abs {mx:.3e} (bound exceeded by {max(over.max(), 0):.3e}), rel L2 {rel:.3e}"
     return mx, rel
+

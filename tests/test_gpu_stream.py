@@ -227,3 +227,39 @@ def test_context_above_bound_reports_bounds(monkeypatch, bad):
         assert torch.isnan(out[bad].float()).all()
         assert_close(out, ref, seqs=keep, what=f"bad length in sequence {bad}, ps{ps}")
     monkeypatch.delenv("PA_DECODE_KERNEL")
+
+
+@pytest.mark.parametrize("T,kv,mode,ps,want", [(1, "bf16", None, 2048, "per_unit"),
+                                                (1, "bf16", None, 256, "persistent"),
+                                                (1, "fp8", None, 2048, "persistent"),
+                                                (5, "bf16", None, 256, "persistent"),
+                                                (5, "bf16", None, 2048, "per_unit"),
+                                                (1, "bf16", "persistent", 2048, "persistent"),
+                                                (5, "fp8", "per_unit", 256, "per_unit"),
+                                                (2, "bf16", "persistent", 256, "per_unit")])
+def test_kernel_choice(monkeypatch, T, kv, mode, ps, want):
+    """Which kernel a call runs (pa_last_attention_kernel): the library's choice and
+    PA_DECODE_KERNEL's override.  The library takes the persistent kernel for FP8 pages,
+    and for bf16 pages when the launch has at least 4 units (bound) per resident CTA: with
+    17 sequences up to 5000 tokens that is 2720 units at 256-token partitions, 408 at
+    2048-token ones, against 456 resident CTAs for 4 rows (304 for 20).  Ten rows per kv
+    head (T = 2, G = 5) are not served by the persistent kernel."""
+    if mode is None:
+        monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("PA_DECODE_KERNEL", mode)
+    hq = 40 if T == 2 else 32
+    w = W.build("stream_which", [max(L, T) for L in LENS], num_q_heads=hq, num_kv_heads=8,
+                head_dim=128, num_query_tokens=T, seed=51)
+    if kv == "fp8":
+        w = W.fp8_variant(w, seed=1)
+        q, kc, vc = to_dev(w.q), to_dev(w.k_codes), to_dev(w.v_codes)
+        pa.verify_fp8(q, kc, vc, to_dev(w.k_scale), to_dev(w.v_scale), to_dev(w.block_tables),
+                      to_dev(w.context_lens), w.max_context_len, w.scale, ps)
+    else:
+        d = Dev(w)
+        d.reshape()
+        d.attend(partition_size=ps)
+    torch.cuda.synchronize()
+    monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+    assert pa.last_attention_kernel() == want

@@ -132,3 +132,14 @@ def test_deterministic():
     a = d.attend(partition_size=0).clone()
     b = d.attend(partition_size=0)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_the_tcgen05_kernel_is_the_one_that_runs():
+    """With PA_VERIFY_KERNEL=tcgen05 the verify tiles run on the tcgen05 kernel (not on
+    the persistent or the one-CTA-per-unit mma.sync kernel)."""
+    w = W.build("tc_which", LENS, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                num_query_tokens=5, seed=17)
+    d = Dev(w)
+    d.reshape()
+    d.attend(partition_size=0)
+    assert pa.last_attention_kernel() == "tcgen05"
