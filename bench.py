@@ -114,18 +114,44 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def strip_comments(src: bytes) -> bytes:
+    """C/C++ source without its comments (string and character literals kept), and
+    without blank lines and trailing spaces: what the compiler sees of the code."""
+    out, i, n = bytearray(), 0, len(src)
+    while i < n:
+        c = src[i:i + 1]
+        if src.startswith(b"//", i):
+            j = src.find(b"\n", i)
+            i = n if j < 0 else j
+        elif src.startswith(b"/*", i):
+            j = src.find(b"*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c in (b'"', b"'"):
+            j = i + 1
+            while j < n and src[j:j + 1] != c:
+                j += 2 if src[j:j + 1] == b"\\" else 1
+            out += src[i:j + 1]
+            i = j + 1
+        else:
+            out += c
+            i += 1
+    lines = [ln.rstrip() for ln in bytes(out).split(b"\n")]
+    return b"\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash():
-    """Hash of what the attention kernel is compiled from: its template, its PTX helpers,
-    and the constants and parameter struct it reads (launcher declarations excluded)."""
+    """Hash of what the attention kernels are compiled from (comments aside): their
+    templates, their PTX helpers, and the constants and parameter struct they read
+    (launcher declarations excluded)."""
     csrc = os.path.join(ROOT, "paged_kv_cache_221_gb300", "csrc")
     h = hashlib.sha256()
     for n in KERNEL_SOURCES:
         with open(os.path.join(csrc, n), "rb") as f:
-            h.update(f.read())
+            h.update(strip_comments(f.read()))
     with open(os.path.join(csrc, KERNEL_PARAMS), "rb") as f:
         text = f.read()
     end = text.find(b"};", text.find(b"struct AttnParams"))
-    h.update(text[:end + 2])
+    h.update(strip_comments(text[:end + 2]))
     return h.hexdigest()[:16]
 
 

@@ -1,5 +1,7 @@
-// Persistent paged attention for decode shapes: per-sequence mode, at most 8
-// query rows per kv head (one n-tile column, NTW = 1), bf16 or FP8 pages.
+// Persistent paged attention, per-sequence mode, bf16 or FP8 pages: decode
+// shapes (at most 8 query rows per kv head: one row column, four page lanes,
+// 3 CTAs per SM) and verify tiles (17-24 rows: three row columns, two page
+// lanes, two ring stages per softmax step, 2 CTAs per SM).
 //
 // The one-CTA-per-unit kernel (pa_attn.cuh) pays a start-up on every work
 // unit: the context length, the block ids and the query rows are fetched before
@@ -14,20 +16,28 @@
 //    in sequence order, then every sequence's last partition, largest first (a
 //    stable counting sort into 32 size classes).  List position i and kv head
 //    h form unit i * Hkv + h; units past a sequence's end do not exist.
-//  * CTA c then takes list units c, 2S - 1 - c, 2S + c, ... (S CTAs): a snake
-//    over the largest-first list, so that the CTAs' totals come out even
-//    without a shared counter.
-//  * The producer warp publishes each unit into one of two records,
-//    with the unit's query rows copied by cp.async into the record's query
-//    buffer, and streams the unit's pages into the ring right behind the
-//    previous unit's.  The next unit is looked up, and its first 32 block ids
-//    requested, when at most two groups of the current unit are left to issue;
-//    each later batch of 32 block ids is requested one batch ahead.
-//  * Consumer warps (page lanes) take the records in order.  At a unit's end
-//    each page lane keeps its last ring stage and writes its (m, l, O) partial
-//    there; the lanes merge through those stages, write the output (one
+//  * CTAs claim list positions from a counter in the split-KV scratch (StreamCtl,
+//    pa_internal.h: the merge that follows each launch resets it), so that an
+//    idle CTA takes the next largest unit.  Without scratch, or on scratch whose
+//    counter is not (yet) known to be reset, CTA c takes positions c,
+//    2S - 1 - c, 2S + c, ... (S CTAs): a snake over the largest-first list.
+//  * The producer warp publishes each unit into one of two records, with the
+//    unit's query rows copied by cp.async into the record's query buffer, and
+//    streams the unit's pages into the ring right behind the previous unit's.
+//    The next claim goes out three issue groups before the end of the current
+//    unit; the next unit is decoded, and its first 32 block ids requested, two
+//    groups before the end; each later batch of 32 block ids is requested one
+//    batch ahead.
+//  * Units start on a multiple of the page-lane count in the ring (the skipped
+//    items pass through empty), so page lane q takes a unit's pages q, q + PL,
+//    ... whichever CTA runs it: the output is bit-identical to the
+//    one-CTA-per-unit kernel's.
+//  * Consumer warps take the records in order.  At a unit's end, with one row
+//    column, each page lane keeps its last ring stage and writes its (m, l, O)
+//    partial there; the lanes merge through those stages, write the output (one
 //    partition) or the split-KV partial, and only then release the kept stages,
 //    so the ring keeps streaming the next unit's first pages during the merge.
+//    With three row columns the partials go to a merge buffer of their own.
 //
 // Partitions, partial slots and the merge kernel that follows are those of the
 // one-CTA-per-unit kernel; the per-page arithmetic is the same function.
