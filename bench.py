@@ -851,6 +851,22 @@ def run_spec_accept_timing(args):
                       "rows": rows}), flush=True)
 
 
+def prefill_slots(n_tokens, n_blocks, block_size, seed):
+    """Slot mapping of a prefill chunk of n_tokens: sequences of 128 .. 2048 tokens (the
+    last one cut at the chunk's end), each filling consecutive slots of distinct, randomly
+    chosen blocks from their first slot."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    blocks = iter(rng.permutation(n_blocks))
+    out = []
+    while len(out) < n_tokens:
+        L = min(int(rng.integers(128, 2049)), n_tokens - len(out))
+        for j in range(0, L, block_size):
+            b = next(blocks)
+            out.extend(range(b * block_size, b * block_size + min(block_size, L - j)))
+    return np.array(out, dtype=np.int64)
+
+
 def run_aux_kernels(args):
     """The hot path's small kernels on their own: reshape_and_cache (bf16 and FP8 pages)
     for one decode step's new tokens and for a prefill-sized chunk, and the copy-on-write
@@ -897,13 +913,20 @@ def run_aux_kernels(args):
                      "gbps": round(gbps, 1), "frac": round(gbps / peak, 4)})
 
     for N, case in ((256, "one 70B-shape decode step: 256 new tokens"),
-                    (16384, "a 16384-token prefill chunk")):
+                    (16384, "a 16384-token prefill chunk (sequences of 128-2048 tokens in "
+                            "consecutive slots)")):
         nb = int(N / BS * 1.25) + 16
         k = torch.zeros(nb, Hkv, BS, D, dtype=torch.bfloat16, device=dev)
         v = torch.zeros_like(k)
         key = torch.randn(N, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
         val = torch.randn(N, Hkv, D, device=dev, generator=g).to(torch.bfloat16)
-        slots = torch.randperm(nb * BS, device=dev, generator=g)[:N].to(torch.int64)
+        if N == 256:
+            # a decode step: one new token per sequence, each at its own slot
+            slots = torch.randperm(nb * BS, device=dev, generator=g)[:N].to(torch.int64)
+        else:
+            # a prefill chunk: sequences of 128 .. 2048 tokens one after another, each
+            # filling consecutive slots of its own randomly placed blocks
+            slots = torch.from_numpy(prefill_slots(N, nb, BS, seed=5)).to(dev)
         vec = N * Hkv * D * 2
         us = timed(lambda: pa.reshape_and_cache(key, val, k, v, slots))
         row("reshape_and_cache_kernel", case, 2 * vec + 2 * vec + N * 8, us)

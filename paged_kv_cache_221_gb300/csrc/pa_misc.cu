@@ -54,7 +54,11 @@ cudaError_t launch_reshape(const void* key, const void* value, void* k_cache, vo
 // One thread per 8 head dims of one (token, kv head): each bf16 value x is
 // stored as the E4M3 code nearest to x / scale[head] (IEEE float32 division,
 // round to nearest even, saturating to +-448).  K pages are token-major
-// [NB, Hkv, 16, D]; V pages are transposed [NB, Hkv, D, 16].
+// [NB, Hkv, 16, D]; V pages are transposed [NB, Hkv, D, 16], so one token's V
+// lands as one byte in each of D rows of 16 bytes.  Consecutive threads take
+// consecutive tokens of the same (kv head, 8 dims): the tokens of a prefill
+// chunk fill consecutive slots, so a warp's V byte stores land in one or two
+// 16-byte rows instead of 32 rows apart.
 
 __global__ void __launch_bounds__(256)
     reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
@@ -67,10 +71,10 @@ __global__ void __launch_bounds__(256)
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long total = static_cast<long long>(num_tokens) * hkv * vecs;
   if (idx >= total) return;
-  const int v = static_cast<int>(idx % vecs);
-  const long long th = idx / vecs;
-  const int h = static_cast<int>(th % hkv);
-  const long long i = th / hkv;
+  const long long i = idx % num_tokens;
+  const long long hv = idx / num_tokens;
+  const int v = static_cast<int>(hv % vecs);
+  const int h = static_cast<int>(hv / vecs);
   const long long s = slots[i];
   if (s < 0) return;                        // padding token
   if (s >= num_slots) {

@@ -168,6 +168,54 @@ def test_quantisation_edge_values_bit_exact():
     np.testing.assert_array_equal(codes(dv), vref)
 
 
+def _prefill_slots(rng, seq_lens, first_offsets, NB, pad_every=0):
+    """Slot mapping of a prefill chunk: each sequence's tokens fill consecutive slots of
+    distinct random blocks, starting at first_offsets[i] inside its first block; a
+    padding token (-1) after every pad_every tokens when pad_every > 0."""
+    blocks = list(rng.permutation(NB))
+    slots = []
+    for L, o in zip(seq_lens, first_offsets):
+        pos = o
+        blk = blocks.pop()
+        for _ in range(L):
+            if pos == 16:
+                blk, pos = blocks.pop(), 0
+            slots.append(blk * 16 + pos)
+            pos += 1
+            if pad_every and len(slots) % pad_every == 0:
+                slots.append(-1)
+    return np.array(slots, dtype=np.int64)
+
+
+@pytest.mark.parametrize("D,hkv", [(128, 8), (128, 1), (64, 2), (96, 2)])
+@pytest.mark.parametrize("layout", ["aligned", "offset", "padded"])
+def test_prefill_chunk_code_for_code(D, hkv, layout):
+    """A prefill chunk: runs of whole blocks written in order (16-byte transposed V rows)
+    next to partial blocks, sequences that start at any token of a 32-token tile, and
+    padding tokens, code for code against the oracle over the whole pool.  head_dim 96
+    takes the byte-wise kernel."""
+    rng = np.random.default_rng(D + hkv)
+    lens = [48, 5, 16, 33, 70, 1, 17, 64, 31]
+    offs = {"aligned": [0] * len(lens), "offset": [3, 0, 9, 15, 0, 7, 0, 1, 12],
+            "padded": [0, 4, 0, 0, 2, 0, 0, 0, 5]}[layout]
+    NB = 64
+    slots = _prefill_slots(rng, lens, offs, NB, pad_every=37 if layout == "padded" else 0)
+    N = len(slots)
+    key = W.normal_bf16(rng, (N, hkv, D))
+    value = W.normal_bf16(rng, (N, hkv, D))
+    k_scale = rng.uniform(0.004, 0.03, size=hkv).astype(np.float32)
+    v_scale = rng.uniform(0.004, 0.03, size=hkv).astype(np.float32)
+    kc = np.full((NB, hkv, 16, D), 0x5A, dtype=np.uint8)
+    vc = np.full((NB, hkv, D, 16), 0xA5, dtype=np.uint8)
+    kref, vref = F.reshape_and_cache(key, value, kc, vc, slots, k_scale, v_scale, 16)
+    dk, dv = to_dev(kc), to_dev(vc)
+    pa.reshape_and_cache_fp8(to_dev(key), to_dev(value), dk, dv, to_dev(slots),
+                             to_dev(k_scale), to_dev(v_scale))
+    np.testing.assert_array_equal(codes(dk), kref)
+    np.testing.assert_array_equal(codes(dv), vref)
+    assert pa.get_device_error() == 0
+
+
 def test_nan_input_stays_nan():
     key = np.full((1, 1, 64), 0x7FC0, dtype=np.uint16)           # bf16 NaN
     value = np.full((1, 1, 64), 0xFFC0, dtype=np.uint16)         # negative NaN
