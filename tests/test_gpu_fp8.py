@@ -314,3 +314,57 @@ def test_shared_prefix_read_once(psize):
     assert_close(out, ref, what=f"fp8 shared prefix ps{psize}")
     plain = d.attend(partition_size=psize)
     assert_close(out, plain.float().cpu().double().numpy(), what="fp8 shared vs plain")
+
+
+def _spread_queries(w, seed):
+    """Query rows of very different magnitudes: each (sequence, token, head) row times
+    2^e, e uniform in [-8, 3]; one row of zeros per sequence; and one row per sequence
+    whose dims fall from 1 to 2^-20 of its largest.  Every row must keep its own
+    scores through the query's conversion for the tensor cores (a per-row factor
+    applied to the wrong row, or lost low-order parts, show here)."""
+    rng = np.random.default_rng(seed)
+    qf = (w.q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    qf *= np.exp2(rng.integers(-8, 4, size=qf.shape[:3]))[..., None]
+    qf[:, 0, 1, :] = 0.0
+    qf[:, -1, 2, :] *= np.exp2(-np.arange(qf.shape[-1]) * 20.0 / qf.shape[-1])
+    w.q = W.f32_to_bf16_bits(qf.astype(np.float32))
+    return w
+
+
+@pytest.mark.parametrize("D,T", [(128, 1), (128, 5), (64, 1), (64, 4), (128, 2)])
+def test_query_rows_of_different_magnitudes(monkeypatch, D, T):
+    """Both attention kernels on spread query rows: within tolerance of the oracle and
+    bit-identical to each other."""
+    lens = [max(L, T) for L in (300, 1000, 17, 2048, 513, 64, 5, 1500)]
+    base = W.build("qmag", lens, num_q_heads=32, num_kv_heads=8, head_dim=D,
+                   num_query_tokens=T, seed=D + 7 * T)
+    w = _spread_queries(W.fp8_variant(base, seed=D + T), seed=D * T)
+    ref, _, _ = F.run_workload(w)
+    d = Dev8(w)
+    d.reshape()
+    for ps in (48, 0):
+        outs = []
+        for mode in ("per_unit", "persistent"):
+            monkeypatch.setenv("PA_DECODE_KERNEL", mode)
+            outs.append(d.attend(partition_size=ps))
+            torch.cuda.synchronize()
+        monkeypatch.delenv("PA_DECODE_KERNEL")
+        for out in outs:
+            assert_close(out, ref, what=f"fp8 query magnitudes D{D} T{T} ps{ps}")
+        np.testing.assert_array_equal(outs[0].cpu().view(torch.int16).numpy(),
+                                      outs[1].cpu().view(torch.int16).numpy())
+
+
+def test_shared_prefix_query_rows_of_different_magnitudes():
+    """The shared-prefix kernel (one CTA carries every member's rows) on spread rows."""
+    w = _spread_queries(shared_fp8(), seed=5)
+    ref, _, _ = F.run_workload(w)
+    d = Dev8(w)
+    d.reshape()
+    sg, gp = to_dev(w.seq_group), to_dev(w.group_prefix_blocks)
+    for psize in (128, 0):
+        out = pa.decode_shared_prefix(d.q, d.k, d.v, d.tables, d.lens, sg, gp,
+                                      w.max_group_size, w.max_prefix_blocks,
+                                      w.max_context_len, w.scale, psize, k_scale=d.ks,
+                                      v_scale=d.vs)
+        assert_close(out, ref, what=f"fp8 shared prefix query magnitudes ps{psize}")
