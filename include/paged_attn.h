@@ -127,7 +127,10 @@ size_t pa_workspace_size(int num_seqs, int num_q_heads, int num_query_tokens,
                          int max_context_len, int head_dim, int block_size, int partition_size,
                          int max_prefix_blocks);
 
-/* Partition size (tokens) that partition_size = 0 selects for this shape. */
+/* Partition size (tokens) that partition_size = 0 selects for this shape, bf16
+ * pages.  Per-sequence calls over FP8 pages select 4096 tokens instead where
+ * this returns 2048 or 3072 (contexts past 4096 tokens, 256 or more (sequence,
+ * kv head) pairs); their scratch need is then at most the bf16 one. */
 int pa_default_partition_size(int num_seqs, int num_kv_heads, int max_context_len,
                               int block_size);
 

@@ -117,7 +117,11 @@ struct Plan {
 // that a small batch still spreads over the whole GPU.  Otherwise: up to 4096
 // tokens, 1536-token partitions; longer contexts, 2048-token partitions, or
 // 3072 when there are many pairs (>= 1024) so that fewer partials need merging.
-int default_partition_tokens(int max_context_len, int num_seqs, int num_kv_heads) {
+// FP8 pages (per-sequence calls) past 4096 tokens: 4096-token partitions (a
+// unit then carries as many bytes as a 2048-token bf16 one; speculative verify
+// measured 4 % faster than with 2048, the 70B-shape batch the same as with 3072).
+int default_partition_tokens(int max_context_len, int num_seqs, int num_kv_heads,
+                             bool fp8_pages = false) {
   if (max_context_len <= 1024) return ceil_div(max_context_len, kBlockSize) * kBlockSize;
   const long long pairs = static_cast<long long>(num_seqs) * num_kv_heads;
   if (pairs > 0 && pairs < 256) {
@@ -127,6 +131,7 @@ int default_partition_tokens(int max_context_len, int num_seqs, int num_kv_heads
     return std::max(ps, 128);
   }
   if (max_context_len <= 4096) return 1536;
+  if (fp8_pages) return 4096;
   if (pairs >= 1024) return 3072;
   return 2048;
 }
@@ -214,7 +219,7 @@ pa_status run_attention(const AttnArgs& a) {
 
   int psize = a.partition_size;
   if (psize == 0) {
-    psize = default_partition_tokens(a.max_context_len, a.num_seqs, a.hkv);
+    psize = default_partition_tokens(a.max_context_len, a.num_seqs, a.hkv, a.kv8 && !grouped);
     Plan probe = make_plan(a.num_seqs, a.hq, a.T, a.max_context_len, a.head_dim, psize,
                            max_prefix);
     if (!grouped && probe.ws_bytes > 0 && a.workspace == nullptr)
@@ -394,7 +399,7 @@ const char* pa_status_string(int status) {
   }
 }
 
-int pa_version(void) { return 101; }
+int pa_version(void) { return 102; }
 
 int pa_last_attention_kernel(void) { return g_last_kernel; }
 

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     for code, name in _lib.STATUS_NAMES.items():
         assert lib.pa_status_string(code).decode() == name
-    assert lib.pa_version() == 101
+    assert lib.pa_version() == 102
 
 
 def test_workspace_size_host_only(lib):
