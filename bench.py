@@ -573,10 +573,11 @@ class Case:
         # output comes back.
         used = set(int(x) for x in w.block_tables.ravel() if x >= 0)
         pad = next(bb for bb in range(w.num_blocks) if bb not in used)
-        rps = self.ps if self.ps > 0 else pa.default_partition_size(
-            w.num_seqs, w.num_kv_heads, w.max_context_len)
+        # partition size 0: the class is captured with the library default, as the
+        # device-timed call uses it
         runner = pa.GraphRunner(self.k, self.v, w.num_q_heads, w.max_context_len,
-                                w.max_blocks_per_seq, pad, rps, classes=(w.num_seqs,),
+                                w.max_blocks_per_seq, pad, max(self.ps, 0),
+                                classes=(w.num_seqs,),
                                 num_query_tokens=T, scale=w.scale, window_size=self.window,
                                 k_scale=self.ks, v_scale=self.vs, host_staging=True)
         # the step's inputs sit in the runner's page-locked host buffers; every replay

@@ -476,7 +476,7 @@ pa_status pa_spec_accept(const float* target_probs, const float* draft_probs,
  * appends may overwrite), then replays graph c on `stream`.  Output rows 0 .. B-1
  * are those of pa_attention with num_seqs = B and the class's partition size:
  * partition_size if > 0, else the library default for num_seqs = c
- * (pa_default_partition_size).  max_context_len is the bound every captured
+ * (pa_default_partition_size, with its FP8 rule for FP8 pages).  max_context_len is the bound every captured
  * launch is sized for.  The workspace must hold the largest need over the
  * classes (pa_workspace_size for each class).  The runner owns
  * one CUDA stream (for capture) and the instantiated graphs, nothing else.

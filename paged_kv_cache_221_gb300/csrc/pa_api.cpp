@@ -370,6 +370,11 @@ pa_status run_attention(const AttnArgs& a) {
 
 namespace pa {
 
+int default_partition_for(int max_context_len, int num_seqs, int num_kv_heads, bool fp8_pages) {
+  if (max_context_len < 1) return kBlockSize;
+  return default_partition_tokens(max_context_len, num_seqs, num_kv_heads, fp8_pages);
+}
+
 size_t workspace_for(int num_seqs, int num_q_heads, int num_kv_heads, int num_query_tokens,
                      int max_context_len, int head_dim, int partition_size,
                      int max_prefix_blocks) {

@@ -70,6 +70,10 @@ struct StreamCtl {
 };
 constexpr unsigned long long kStreamTag = 0x70615F7374726D31ull;
 
+// The partition size (tokens) a per-sequence call with partition_size 0 uses:
+// the library default for this batch, with the FP8-page rule when fp8_pages.
+int default_partition_for(int max_context_len, int num_seqs, int num_kv_heads, bool fp8_pages);
+
 // Split-KV scratch bytes a call with these sizes needs (partition_size 0 = the
 // library default for this kv-head count).
 size_t workspace_for(int num_seqs, int num_q_heads, int num_kv_heads, int num_query_tokens,

@@ -37,11 +37,12 @@ struct pa_graph_runner {
 namespace {
 
 // The partition size a class is captured with: the configured one, or the library
-// default for that batch size.
+// default for that batch size and page format.
 int partition_for(const pa_runner_config& c, int num_seqs) {
-  return c.partition_size > 0 ? c.partition_size
-                              : pa_default_partition_size(num_seqs, c.num_kv_heads,
-                                                          c.max_context_len, c.block_size);
+  return c.partition_size > 0
+             ? c.partition_size
+             : pa::default_partition_for(c.max_context_len, num_seqs, c.num_kv_heads,
+                                         c.kv_dtype == PA_KV_FP8_E4M3);
 }
 
 bool staged(const pa_runner_buffers& b) {
