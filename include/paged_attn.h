@@ -230,7 +230,9 @@ pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* k_c
  * not supported, smaller ones lose the bits below 2^-24) and the softmax
  * weights are rounded to f16 before they multiply V.  Workspace, partitions,
  * requirements and errors as pa_decode / pa_verify, plus k_scale, v_scale
- * non-NULL.
+ * non-NULL; partition_size 0 selects the FP8 rule of pa_default_partition_size
+ * (4096-token partitions past 4096-token contexts), whose scratch need is at
+ * most pa_workspace_size's.
  */
 pa_status pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                         const float* k_scale, const float* v_scale, const int32_t* block_tables,
