@@ -368,3 +368,22 @@ def test_shared_prefix_query_rows_of_different_magnitudes():
                                       w.max_context_len, w.scale, psize, k_scale=d.ks,
                                       v_scale=d.vs)
         assert_close(out, ref, what=f"fp8 shared prefix query magnitudes ps{psize}")
+
+
+def test_default_partition_for_long_contexts():
+    """FP8 pages past 4096-token contexts default to 4096-token partitions: a scratch
+    sized for them is enough with partition_size 0 (the bf16 default, 2048 tokens,
+    would need more and be refused), and the result is that of an explicit 4096."""
+    w = fp8("spec_verify", "full")
+    d = Dev8(w)
+    d.reshape()
+    need4096 = pa.workspace_size(w.num_seqs, w.num_q_heads, w.num_query_tokens,
+                                 w.max_context_len, w.head_dim, 16, 4096, 0)
+    need2048 = pa.workspace_size(w.num_seqs, w.num_q_heads, w.num_query_tokens,
+                                 w.max_context_len, w.head_dim, 16, 2048, 0)
+    assert need4096 < need2048
+    ws = torch.empty(need4096, dtype=torch.uint8, device="cuda")
+    out0 = d.attend(partition_size=0, workspace=ws)
+    out4096 = d.attend(partition_size=4096, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out0.view(torch.int16), out4096.view(torch.int16))
